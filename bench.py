@@ -1,0 +1,400 @@
+#!/usr/bin/env python3
+"""Benchmark of the causal GQA prefill attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 3] [--impl ours|reference]
+
+One step = one forward pass (the whole hot path: one kernel launch) over the
+workload's synthetic bf16 inputs, already resident in device memory. L2 is
+flushed (a 256 MiB device write) before every step, outside the timed
+interval; each step is timed with CUDA events on the launching stream. The
+default workload is the Llama-3-8B-shaped layer (B=1, L=8192, n_q=32,
+n_kv=8, d_h=128), the first of the model-shaped workloads at L >= 8192.
+
+Under torchrun (N > 1) every rank runs its own replica of the workload on its
+own GPU (units are independent; no collective on the data path): "scaling"
+is weak and ``value`` is the total over ranks divided by the slowest rank's
+time. Rank 0 prints one JSON line.
+
+``--impl reference`` times the fp64 CPU oracle instead (rank 0 only), each
+step a bounded sample of query rows of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "causal prefill attention TFLOP/s (2·n_q·d_h·L²) on 1 GB300; % of bf16 peak"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCE = os.path.join(ROOT, "causal_gqa_prefill_gb300", "csrc", "attn_prefill.cu")
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+class Dist:
+    def __init__(self):
+        self.world = _env_int("WORLD_SIZE", 1)
+        self.rank = _env_int("RANK", 0)
+        self.local_rank = _env_int("LOCAL_RANK", 0)
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")   # host-side barrier / max only
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.remove(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        peak_power = max(r[2] for r in rows)
+        loaded = [r for r in rows if r[2] >= 0.5 * peak_power] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": peak_power}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"bf16_tflops": FALLBACK_BF16_TFLOPS}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(workload_number: int):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.tsv")
+    if not os.path.exists(path):
+        return None
+    src = kernel_source_hash()
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            parts = line.split("\t")
+            if len(parts) >= 3 and parts[0] == str(workload_number) and parts[1] == src:
+                return float(parts[2])
+    return None
+
+
+def oracle_sample(w, q_host, k_host, v_host, rng, rows_per_chunk, seconds=None, chunks=None):
+    """Times the fp64 oracle on random query rows; returns (flops, seconds, rows)."""
+    import numpy as np
+    import oracle
+
+    flops = 0.0
+    spent = 0.0
+    nrows = 0
+    done = 0
+    while True:
+        b = rng.integers(0, w.B, rows_per_chunk)
+        h = rng.integers(0, w.n_q, rows_per_chunk)
+        i = rng.integers(0, w.L, rows_per_chunk)
+        rows = np.stack([b, h, i], axis=1)
+        qv = q_host[b, i, h]
+        t0 = time.perf_counter()
+        oracle.attention_rows(qv, k_host, v_host, rows, causal=w.causal, scale=w.scale, n_q=w.n_q)
+        spent += time.perf_counter() - t0
+        keys = (i + 1) if w.causal else np.full_like(i, w.L)
+        flops += float((4.0 * w.d_h * keys).sum())
+        nrows += rows_per_chunk
+        done += 1
+        if seconds is not None and spent >= seconds:
+            break
+        if chunks is not None and done >= chunks:
+            break
+    return flops, spent, nrows
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [p.get("num_threads") for p in threadpool_info() if p.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def host_inputs(w):
+    """The workload's seeded inputs as float64 host arrays (drawn on the GPU if one
+    is present, exactly as the CUDA path sees them)."""
+    import numpy as np
+    import torch
+    from causal_gqa_prefill_gb300 import workloads as W
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    q, k, v = W.make_inputs(w, dev)
+    f = lambda t: t.float().cpu().numpy().astype(np.float64)
+    return f(q), f(k), f(v)
+
+
+def run_reference(args, w, dist):
+    import numpy as np
+
+    if dist.rank != 0:
+        return 0
+    q, k, v = host_inputs(w)
+    rng = np.random.default_rng(w.seed)
+    rows_per_step = args.ref_rows
+    for _ in range(args.warmup):
+        oracle_sample(w, q, k, v, rng, rows_per_step, chunks=1)
+    total_flops, total_s = 0.0, 0.0
+    step_ms = []
+    for _ in range(args.steps):
+        f, s, _ = oracle_sample(w, q, k, v, rng, rows_per_step, chunks=1)
+        total_flops += f
+        total_s += s
+        step_ms.append(s * 1e3)
+    value = total_flops / total_s / 1e12
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(step_ms),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": dict(w.describe()),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{rows_per_step} random query rows per step of {w.name}; "
+                                   "fp64 NumPy oracle on the host cores"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w, dist):
+    import numpy as np
+    import torch
+    import causal_gqa_prefill_gb300 as cg
+    from causal_gqa_prefill_gb300 import workloads as W
+
+    from causal_gqa_prefill_gb300 import build
+    build.build()
+    torch.cuda.set_device(dist.local_rank)
+    dev = torch.device("cuda", dist.local_rank)
+    q, k, v = W.make_inputs(w, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.n_q, w.L), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = int(stream.cuda_stream)
+
+    def step():
+        st = cg.attn_prefill_fwd(q, k, v, o, lse, w.B, w.L, w.n_q, w.n_kv, w.d_h, int(w.causal),
+                                 w.scale, sh)
+        if st != cg.ATTN_OK:
+            raise cg.AttnError(st, "attn_prefill_fwd")
+
+    sampler = ClockSampler(dist.local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    sampler.start()
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    st = cg.attn_device_check(sh)
+    if st != cg.ATTN_OK:
+        raise cg.AttnError(st, "warm-up")
+
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    dist.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for s, e in events:
+        flush.zero_()
+        s.record(stream)
+        step()
+        e.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    t_wall = time.perf_counter() - t_wall
+    clocks = sampler.stop()
+    st = cg.attn_device_check(sh)
+    if st != cg.ATTN_OK:
+        raise cg.AttnError(st, "timed steps")
+    step_ms = [s.elapsed_time(e) for s, e in events]
+    mean_ms = dist.max(statistics.mean(step_ms))
+    flops = w.metric_flops()
+    value = dist.world * flops / (mean_ms * 1e-3) / 1e12
+
+    # end to end: pinned host inputs -> device, forward, outputs -> pinned host
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        e2e_step()
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    dist.barrier()
+    torch.cuda.synchronize()
+    for s, e in ev2:
+        flush.zero_()
+        s.record(stream)
+        e2e_step()
+        e.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    e2e_ms = dist.max(statistics.mean(s.elapsed_time(e) for s, e in ev2))
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    e2e_value = dist.world * flops / (e2e_ms * 1e-3) / 1e12
+
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    achieved = flops / (statistics.mean(step_ms) * 1e-3) / 1e12
+    traffic = recorded_traffic(w.number)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": dict(w.describe(), parallelism=f"replicas x{dist.world}",
+                       l2="flushed before every step (256 MiB device write, outside the timed interval)"),
+        "pct_of_bf16_peak": 100.0 * achieved / peak,
+        "gbs_io": w.io_bytes() / (statistics.mean(step_ms) * 1e-3) / 1e9,
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak, "peak_source": f"bf16_tflops ({peak_src}, burst)",
+                     "traffic": traffic},
+        "step_ms_min": min(step_ms), "wall_s_timed": t_wall,
+        "grid": cg.attn_prefill_grid_size(w.B, w.L, w.n_q, w.n_kv, w.d_h, w.causal),
+    }
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        fq, fk, fv = (t.float().cpu().numpy().astype(np.float64) for t in (q, k, v))
+        rng = np.random.default_rng(w.seed)
+        f, s, n = oracle_sample(w, fq, fk, fv, rng, 256, seconds=args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": f / s / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{n} random query rows of {w.name} (fp64 NumPy oracle), {s:.1f} s"}
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-rows", type=int, default=512)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from causal_gqa_prefill_gb300 import workloads as W
+    w = W.WORKLOADS[args.workload]
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, w, dist)
+        return run_ours(args, w, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,18 @@
+"""GB300-native causal GQA prefill attention (forward).
+
+The computation runs in a hand-written sm_103a CUDA library
+(``lib/libattn_prefill.so``, C ABI in ``include/attn_prefill.h``); this
+package is a thin binding plus the seeded workload generators. Importing it
+does not load the library; the first call does, and raises if it is missing.
+"""
+
+from ._abi import (ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA,
+                   ATTN_ERR_TIMEOUT, load as load_library, library_path, status_string)
+from .api import (AttnError, attn_prefill, attn_prefill_fwd, attn_device_check,
+                  attn_prefill_grid_size)
+
+__all__ = [
+    "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_CUDA",
+    "ATTN_ERR_TIMEOUT", "AttnError", "attn_prefill", "attn_prefill_fwd", "attn_device_check",
+    "attn_prefill_grid_size", "load_library", "library_path", "status_string",
+]

@@ -1,0 +1,96 @@
+"""Python entry points over the C ABI (torch supplies device memory and streams).
+
+``attn_prefill_fwd`` mirrors the C function argument for argument; the
+convenience wrapper ``attn_prefill`` allocates the outputs and derives the
+sizes from the tensors. Both only marshal arguments: the attention forward
+runs entirely in the CUDA library, and a status other than ATTN_OK raises.
+"""
+
+from __future__ import annotations
+
+import math
+
+from . import _abi
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {_abi.status_string(status)}")
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def attn_prefill_fwd(q, k, v, o, lse, B, L, n_q, n_kv, d_h, causal, scale, stream=None) -> int:
+    """Direct call of the C entry point; returns the raw status code.
+
+    q, k, v, o, lse are CUDA tensors or integer device addresses with the
+    layouts of the C header; ``stream`` is a torch.cuda.Stream, a raw
+    cudaStream_t as int, or None for torch's current stream.
+    """
+    lib = _abi.load()
+    return int(lib.attn_prefill_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(L),
+                                    int(n_q), int(n_kv), int(d_h), int(causal), float(scale),
+                                    _stream_handle(stream)))
+
+
+def attn_device_check(stream=None) -> int:
+    """Synchronise the stream and report device-side timeouts (raw status)."""
+    return int(_abi.load().attn_device_check(_stream_handle(stream)))
+
+
+def attn_prefill_grid_size(B, L, n_q, n_kv, d_h, causal=True) -> int:
+    return int(_abi.load().attn_prefill_grid_size(int(B), int(L), int(n_q), int(n_kv), int(d_h),
+                                                  int(bool(causal))))
+
+
+def attn_prefill(q, k, v, *, causal: bool = True, scale: float | None = None, out=None, lse=None,
+                 stream=None):
+    """O, LSE = attention(q, k, v) for bf16 CUDA tensors q [B,L,n_q,d], k/v [B,L,n_kv,d].
+
+    Returns (o bf16 [B, L, n_q, d], lse fp32 [B, n_q, L]). ``scale`` defaults
+    to 1/sqrt(d). Outputs may be passed in (``out``, ``lse``) to avoid
+    allocation. The call is asynchronous on ``stream`` (default: current).
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be bfloat16")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B, L, H, d_h] tensor")
+    B, L, n_q, d = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[1] != L or k.shape[3] != d:
+        raise ValueError("k and v must be [B, L, n_kv, d_h] matching q")
+    n_kv = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if lse is None:
+        lse = torch.empty((B, n_q, L), dtype=torch.float32, device=q.device)
+    elif tuple(lse.shape) != (B, n_q, L) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, n_q, L] tensor")
+    st = attn_prefill_fwd(q, k, v, out, lse, B, L, n_q, n_kv, d, int(bool(causal)), scale, stream)
+    if st != _abi.ATTN_OK:
+        raise AttnError(st, "attn_prefill_fwd")
+    return out, lse

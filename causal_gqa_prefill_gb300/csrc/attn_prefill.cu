@@ -1,0 +1,693 @@
+// attn_prefill.cu — causal GQA prefill attention forward for GB300 (sm_103a).
+//
+// One persistent, warp-specialised kernel computes O = softmax(scale*Q K^T +
+// causal mask) V tile by tile with an online softmax, so the L x L scores live
+// only in tensor memory ("Long-Context Attention Explained" (sevydevy),
+// sections "Tiling" and "Online softmax"; "Why Attention Scaling Breaks"
+// (shivam2003), section "Flash Attention: the tiling insight").
+//
+// Work unit: two 128-row query tiles that read the same K/V head (two heads of
+// one GQA group at the same query tile, or, when a group has one head, two
+// neighbouring tiles of that head). Each K/V tile is fetched once by TMA and
+// used by both query tiles ("prefill-attention" flop record (phantomic12),
+// "Arithmetic intensity": GQA raises reuse of every K/V byte by g). Causal
+// units visit only key tiles 0..i (skipping fully masked tiles, "Long-Context
+// Attention Explained", FlashAttention-2 paragraph on causal block skipping),
+// and units are handed out longest first over a persistent grid.
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax for query tile 0     (thread = tile row = TMEM lane)
+//   warps 4-7  softmax for query tile 1
+//   warp  8    TMA producer (Q tiles, K/V ring)
+//   warp  9    tcgen05 MMA issuer; owns the TMEM allocation
+// Tensor memory (512 columns x 128 lanes, fp32):
+//   [0,128)   S0 scores, later P0 (bf16, packed two per column, cols 0..63)
+//   [128,256) S1 / P1
+//   [256,384) O0 accumulator (D columns)
+//   [384,512) O1 accumulator
+//
+// MMA issue order per key tile j (ping-pong between the two query tiles, so
+// one tile's softmax overlaps the other tile's matrix products):
+//   S0_j = Q0 K_j^T ; O1 += P1_{j-1} V_{j-1} ; S1_j = Q1 K_j^T ; O0 += P0_j V_j
+// tcgen05 operations from one thread execute in issue order, so a commit that
+// signals S_t,j ready also implies O_t holds every tile before j.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "attn_prefill.h"
+#include "sm103_ptx.cuh"
+
+namespace {
+
+using namespace gb300;
+
+constexpr int kBM = 128;          // query rows per tile (= TMEM lanes)
+constexpr int kBN = 128;          // keys per K/V tile
+constexpr int kThreads = 320;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384;
+// A row's running maximum is only moved (and O rescaled) once the tile maximum
+// exceeds it by this many log2 units; exponentials stay <= 2^8 meanwhile, and
+// the final O / l and LSE use the same stale maximum, so the result is exact.
+constexpr float kRescaleThreshold = 8.0f;
+constexpr int kStatusTimeout = 1;
+constexpr long long kSpinLimitCycles = 1ll << 31;   // about a second at 2 GHz
+
+template <int D>
+struct Tile {
+  static constexpr int kChunks = D / 64;               // 128-byte swizzle column chunks
+  static constexpr int kQBytes = kBM * D * 2;
+  static constexpr int kKVBytes = kBN * D * 2;
+  static constexpr int kStages = (D == 128) ? 4 : 8;   // K/V ring depth (K and V share it)
+  static constexpr int kSmemBytes = 2 * kQBytes + kStages * kKVBytes + 1024;
+};
+
+struct Params {
+  uint16_t* o;          // bf16 [B, L, n_q, D]
+  float* lse;           // fp32 [B, n_q, L]
+  int* status;          // per-device status word
+  int L, n_q, n_kv, g, T;
+  int causal;
+  int scale_pos;        // 1 when c > 0
+  float c;              // scale * log2(e)
+  int groups;           // B * n_kv
+  int units;            // pairs per group * groups
+  long long spin_limit;
+};
+
+struct Ctl {
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[8], kv_empty[8];
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct Unit {
+  int b, kvh, nkv;
+  int head[2], qtile[2], n[2];
+};
+
+// Unit u -> (batch, K/V head, two query tiles). Units are ordered by pair
+// index first, so ascending u means descending causal length (longest first).
+// Within one (b, kv-head) group the g*T query tiles are listed longest first
+// and paired neighbour by neighbour: slot 1 holds the longer (or equal) tile,
+// slot 0 the next one, and their key-tile counts differ by at most one.
+__device__ __forceinline__ Unit decode_unit(int u, const Params& p) {
+  Unit x;
+  const int pair = u / p.groups;
+  const int grp = u - pair * p.groups;
+  x.b = grp / p.n_kv;
+  x.kvh = grp - x.b * p.n_kv;
+  const int total = p.g * p.T;
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int k = 2 * pair + (1 - s);
+    if (k < total) {
+      const int i = p.T - 1 - k / p.g;
+      x.head[s] = x.kvh * p.g + (k % p.g);
+      x.qtile[s] = i;
+      x.n[s] = p.causal ? i + 1 : p.T;
+    } else {
+      x.head[s] = 0;
+      x.qtile[s] = 0;
+      x.n[s] = 0;
+    }
+  }
+  x.nkv = x.n[1];
+  return x;
+}
+
+// Bounded wait: true when the phase completed; false if another role aborted
+// or this wait ran past the limit (then it raises the abort flag and the
+// device status word so the host sees ATTN_ERR_TIMEOUT).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, Ctl& ctl,
+                                           const Params& p) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = clock64_now();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*reinterpret_cast<volatile int*>(&ctl.abort)) return false;
+    if (static_cast<long long>(clock64_now() - t0) > p.spin_limit) {
+      *reinterpret_cast<volatile int*>(&ctl.abort) = 1;
+      atomicOr(p.status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+// Wait used only while draining after an abort: ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const Params& p) {
+  const uint64_t t0 = clock64_now();
+  while (!mbar_try_wait(bar, parity)) {
+    if (static_cast<long long>(clock64_now() - t0) > p.spin_limit) return;
+  }
+}
+
+// ------------------------------------------------------------------ producer
+
+template <int D>
+__device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                          const CUtensorMap* tmV, Ctl& ctl, const Params& p,
+                          uint32_t sQ0, uint32_t sQ1, uint32_t sKV) {
+  using TL = Tile<D>;
+  uint32_t it = 0;       // K/V ring items issued
+  uint32_t q_issued = 0;
+  bool ok = true;
+  int uc = 0;
+  for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++uc) {
+    const Unit x = decode_unit(u, p);
+    if (uc > 0 && !wait_phase(smem_addr(&ctl.q_empty), (uc - 1) & 1, ctl, p)) { ok = false; break; }
+    const uint32_t qbar = smem_addr(&ctl.q_full);
+    mbar_arrive_expect_tx(qbar, (x.n[0] > 0 ? 2u : 1u) * TL::kQBytes);
+    ++q_issued;
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      if (x.n[s] == 0) continue;
+      const uint32_t dst = s ? sQ1 : sQ0;
+#pragma unroll
+      for (int c = 0; c < TL::kChunks; ++c)
+        tma_load_4d(dst + c * kBM * 128, tmQ, qbar, c * 64, x.head[s], x.qtile[s] * kBM, x.b);
+    }
+    for (int j = 0; j < x.nkv && ok; ++j) {
+#pragma unroll
+      for (int kind = 0; kind < 2; ++kind) {
+        const uint32_t slot = it % TL::kStages, use = it / TL::kStages;
+        if (use > 0 && !wait_phase(smem_addr(&ctl.kv_empty[slot]), (use - 1) & 1, ctl, p)) {
+          ok = false;
+          break;
+        }
+        const uint32_t bar = smem_addr(&ctl.kv_full[slot]);
+        const uint32_t dst = sKV + slot * TL::kKVBytes;
+        mbar_arrive_expect_tx(bar, TL::kKVBytes);
+#pragma unroll
+        for (int c = 0; c < TL::kChunks; ++c)
+          tma_load_4d(dst + c * kBN * 128, kind ? tmV : tmK, bar, c * 64, x.kvh, j * kBN, x.b);
+        ++it;
+      }
+    }
+    if (!ok) break;
+  }
+  if (!ok) {
+    // Let every copy this thread started land before the CTA can exit.
+    if (q_issued) drain_wait(smem_addr(&ctl.q_full), (q_issued - 1) & 1, p);
+    for (uint32_t s = 0; s < TL::kStages && s < it; ++s) {
+      const uint32_t last = s + ((it - 1 - s) / TL::kStages) * TL::kStages;
+      drain_wait(smem_addr(&ctl.kv_full[s]), (last / TL::kStages) & 1, p);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- MMA issuer
+
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    // K step kk: 16 bf16 = 32 bytes inside chunk kk/4 of the swizzled tile.
+    const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+    mma_ss(d_tmem, sdesc_sw128(q_smem + off, 16, 1024), sdesc_sw128(k_smem + off, 16, 1024),
+           idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                         bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, true);
+#pragma unroll
+  for (int kk = 0; kk < kBN / 16; ++kk) {
+    // V tile is [keys][D] with D contiguous (MN-major for this product): 16
+    // keys = 2048 bytes per K step; 64-column chunks are kBN*128 bytes apart.
+    const uint64_t b = sdesc_sw128(v_smem + kk * 16 * 128, kBN * 128, 1024);
+    mma_ts(d_tmem, p_tmem + kk * 8, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ void mma_role(Ctl& ctl, const Params& p, uint32_t tmem, uint32_t sQ0, uint32_t sQ1,
+                         uint32_t sKV) {
+  using TL = Tile<D>;
+  uint32_t it = 0;
+  uint32_t ph_p0 = 0, ph_p1 = 0;
+  int uc = 0;
+  for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++uc) {
+    const Unit x = decode_unit(u, p);
+    if (!wait_phase(smem_addr(&ctl.q_full), uc & 1, ctl, p)) break;
+    tc_fence_after_sync();
+    uint32_t v_prev = 0;
+    bool ok = true;
+    for (int j = 0; j < x.nkv; ++j) {
+      const uint32_t ks = it % TL::kStages;
+      if (!wait_phase(smem_addr(&ctl.kv_full[ks]), (it / TL::kStages) & 1, ctl, p)) { ok = false; break; }
+      ++it;
+      tc_fence_after_sync();
+      const uint32_t k_smem = sKV + ks * TL::kKVBytes;
+      if (j < x.n[0]) {
+        issue_qk<D>(tmem + kColS0, sQ0, k_smem);
+        mma_commit(smem_addr(&ctl.s_full[0]));
+      }
+      if (j > 0) {
+        if (!wait_phase(smem_addr(&ctl.p_full[1]), ph_p1, ctl, p)) { ok = false; break; }
+        ph_p1 ^= 1;
+        tc_fence_after_sync();
+        issue_pv<D>(tmem + kColO1, tmem + kColS1, sKV + v_prev * TL::kKVBytes, j - 1 > 0);
+        mma_commit(smem_addr(&ctl.kv_empty[v_prev]));
+      }
+      issue_qk<D>(tmem + kColS1, sQ1, k_smem);
+      mma_commit(smem_addr(&ctl.s_full[1]));
+      mma_commit(smem_addr(&ctl.kv_empty[ks]));
+      if (j == x.nkv - 1) mma_commit(smem_addr(&ctl.q_empty));
+
+      const uint32_t vs = it % TL::kStages;
+      if (!wait_phase(smem_addr(&ctl.kv_full[vs]), (it / TL::kStages) & 1, ctl, p)) { ok = false; break; }
+      ++it;
+      tc_fence_after_sync();
+      if (j < x.n[0]) {
+        if (!wait_phase(smem_addr(&ctl.p_full[0]), ph_p0, ctl, p)) { ok = false; break; }
+        ph_p0 ^= 1;
+        tc_fence_after_sync();
+        issue_pv<D>(tmem + kColO0, tmem + kColS0, sKV + vs * TL::kKVBytes, j > 0);
+        if (j == x.n[0] - 1) mma_commit(smem_addr(&ctl.o_done[0]));
+      }
+      v_prev = vs;
+    }
+    if (!ok) break;
+    if (!wait_phase(smem_addr(&ctl.p_full[1]), ph_p1, ctl, p)) break;
+    ph_p1 ^= 1;
+    tc_fence_after_sync();
+    issue_pv<D>(tmem + kColO1, tmem + kColS1, sKV + v_prev * TL::kKVBytes, x.nkv - 1 > 0);
+    mma_commit(smem_addr(&ctl.o_done[1]));
+    mma_commit(smem_addr(&ctl.kv_empty[v_prev]));
+  }
+  // No MMA may still be running when TMEM is released.
+  mma_commit(smem_addr(&ctl.drain));
+  drain_wait(smem_addr(&ctl.drain), 0, p);
+}
+
+// ------------------------------------------------------------------- softmax
+
+__device__ __forceinline__ float fmax8(const float* v) {
+  return fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])),
+               fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
+}
+
+template <int D>
+__device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = (warp & 3) * 32 + lane;                         // tile row = TMEM lane
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+  const uint32_t tS = lane_base + (slot ? kColS1 : kColS0);
+  const uint32_t tO = lane_base + (slot ? kColO1 : kColO0);
+  const uint32_t bar_s = smem_addr(&ctl.s_full[slot]);
+  const uint32_t bar_p = smem_addr(&ctl.p_full[slot]);
+  const uint32_t bar_o = smem_addr(&ctl.o_done[slot]);
+  const float cc = p.scale_pos ? p.c : 1.0f;
+  uint32_t ph_s = 0, ph_o = 0;
+
+  for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+    const Unit x = decode_unit(u, p);
+    const int n = x.n[slot];
+    if (n == 0) continue;
+    const int row = x.qtile[slot] * kBM + r;
+    float m_run = -INFINITY, l_run = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      if (!__all_sync(0xffffffffu, wait_phase(bar_s, ph_s, ctl, p))) { ok = false; break; }
+      ph_s ^= 1;
+      tc_fence_after_sync();
+      uint32_t sr[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
+      tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(sr));
+      tmem_after_wait(*reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+      tmem_after_wait(*reinterpret_cast<uint32_t(*)[32]>(sr + 64));
+      tmem_after_wait(*reinterpret_cast<uint32_t(*)[32]>(sr + 96));
+      float s[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i]);
+      if (!p.scale_pos) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) s[i] *= p.c;
+      }
+      if (j == n - 1) {
+        if (p.causal) {
+          // Diagonal tile: key index kBN*j + i against query kBM*qtile + r.
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (i > r) s[i] = -INFINITY;
+        } else if (p.L - j * kBN < kBN) {
+          const int lim = p.L - j * kBN;
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (i >= lim) s[i] = -INFINITY;
+        }
+      }
+      float mx8[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) mx8[t] = s[t];
+#pragma unroll
+      for (int i = 8; i < 128; i += 8)
+#pragma unroll
+        for (int t = 0; t < 8; ++t) mx8[t] = fmaxf(mx8[t], s[i + t]);
+      const float m_tile = fmax8(mx8) * cc;
+      const float m_new = fmaxf(m_run, m_tile);
+      const bool need = m_new > m_run + kRescaleThreshold;
+      float alpha = 1.0f;
+      if (need) {
+        alpha = ex2_approx(m_run - m_new);
+        m_run = m_new;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t ov[32];
+          tmem_ld32(tO + c, ov);
+          tmem_wait_ld(ov);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tmem_st32(tO + c, ov);
+        }
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+      // P = 2^(c*s - m) as bf16 pairs into columns [0, 64) of this tile's S
+      // region (every score of the row is already in registers).
+      float sum0 = 0.0f, sum1 = 0.0f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2_approx(fmaf(s[64 * h + 2 * i], cc, -m_use));
+          const float p1 = ex2_approx(fmaf(s[64 * h + 2 * i + 1], cc, -m_use));
+          sum0 += p0;
+          sum1 += p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(tS + 32 * h, pk);
+      }
+      l_run = l_run * alpha + (sum0 + sum1);
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(bar_p);
+    }
+    if (!ok) return;
+    // Epilogue: O = acc / l (bf16, round to nearest even) and LSE in natural log.
+    if (!__all_sync(0xffffffffu, wait_phase(bar_o, ph_o, ctl, p))) return;
+    ph_o ^= 1;
+    tc_fence_after_sync();
+    const float inv_l = 1.0f / l_run;
+    const bool valid = row < p.L;
+    uint16_t* orow = p.o + ((static_cast<size_t>(x.b) * p.L + row) * p.n_q + x.head[slot]) *
+                               static_cast<size_t>(D);
+#pragma unroll
+    for (int c = 0; c < D; c += 32) {
+      uint32_t ov[32];
+      tmem_ld32(tO + c, ov);
+      tmem_wait_ld(ov);
+      uint32_t w[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        w[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
+      if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+      }
+    }
+    if (valid) {
+      const float m_fin = (m_run == -INFINITY) ? 0.0f : m_run;
+      p.lse[(static_cast<size_t>(x.b) * p.n_q + x.head[slot]) * p.L + row] =
+          (m_fin + log2f(l_run)) * 0.69314718055994530942f;
+    }
+  }
+}
+
+// -------------------------------------------------------------------- kernel
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
+                        const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const Params p) {
+  using TL = Tile<D>;
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ Ctl ctl;
+  const uint32_t base = (smem_addr(dyn_smem) + 1023u) & ~1023u;   // swizzle atoms need 1 KiB
+  const uint32_t sQ0 = base, sQ1 = base + TL::kQBytes, sKV = base + 2 * TL::kQBytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&ctl.q_full), 1);
+    mbar_init(smem_addr(&ctl.q_empty), 1);
+    for (int s = 0; s < TL::kStages; ++s) {
+      mbar_init(smem_addr(&ctl.kv_full[s]), 1);
+      mbar_init(smem_addr(&ctl.kv_empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_addr(&ctl.s_full[s]), 1);
+      mbar_init(smem_addr(&ctl.p_full[s]), 128);
+      mbar_init(smem_addr(&ctl.o_done[s]), 1);
+    }
+    mbar_init(smem_addr(&ctl.drain), 1);
+    ctl.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_addr(&ctl.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = ctl.tmem_base;
+
+  if (warp == kLoadWarp) {
+    if (lane == 0) load_role<D>(&tmQ, &tmK, &tmV, ctl, p, sQ0, sQ1, sKV);
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) mma_role<D>(ctl, p, tmem, sQ0, sQ1, sKV);
+  } else {
+    softmax_role<D>(warp >> 2, ctl, p, tmem);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  int* status = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+
+attn_status_t device_state(cudaStream_t stream, DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;   // built for sm_103a only
+    if (!g_encode) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return ATTN_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    if (cudaFuncSetAttribute(attn_prefill_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Tile<64>::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_prefill_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Tile<128>::kSmemBytes) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    int* status = nullptr;
+    if (cudaMalloc(&status, 256) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaMemsetAsync(status, 0, 256, stream) != cudaSuccess) {
+      cudaFree(status);
+      return ATTN_ERR_CUDA;
+    }
+    st.sms = sms;
+    st.status = status;
+    st.ready = true;
+  }
+  *out = &st;
+  return ATTN_OK;
+}
+
+// [B, L, H, D] bf16 as a 4-D tensor (D, H, L, B); boxes of 64 x 1 x 128 x 1
+// with 128-byte swizzle. Rows past L read as zeros.
+bool encode_bhld(CUtensorMap* map, const void* ptr, int D, int H, int64_t L, int64_t B) {
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(H) * D * 2,
+                                 static_cast<cuuint64_t>(L) * H * D * 2};
+  const cuuint32_t box[4] = {64, 1, kBM, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides,
+                  box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Sizes -> work units; returns false when they exceed 32-bit tile indexing.
+bool count_units(int64_t B, int64_t L, int32_t n_q, int32_t n_kv, int* T_out, int* units_out) {
+  const int64_t T = (L + kBM - 1) / kBM;
+  const int64_t g = n_q / n_kv;
+  const int64_t pairs = (g * T + 1) / 2;
+  const int64_t units = pairs * B * n_kv;
+  if (L > (int64_t{1} << 30) || B > (int64_t{1} << 30) || g * T > INT32_MAX ||
+      units > INT32_MAX || B * n_kv > INT32_MAX)
+    return false;
+  *T_out = static_cast<int>(T);
+  *units_out = static_cast<int>(units);
+  return true;
+}
+
+attn_status_t validate(const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, int64_t B, int64_t L, int32_t n_q, int32_t n_kv,
+                       int32_t d_h, int32_t causal, float scale) {
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || L < 1 || n_q < 1 || n_kv < 1 || n_q % n_kv != 0) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  auto misaligned = [](const void* ptr, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0;
+  };
+  if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(o, 16) ||
+      misaligned(lse, 4))
+    return ATTN_ERR_INVALID_ARG;
+  if (d_h != 64 && d_h != 128) return ATTN_ERR_UNSUPPORTED;
+  int T = 0, units = 0;
+  if (!count_units(B, L, n_q, n_kv, &T, &units)) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_prefill_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int64_t B, int64_t L, int32_t n_q, int32_t n_kv, int32_t d_h,
+                               int32_t causal, float scale, void* stream_ptr) {
+  const attn_status_t bad = validate(q, k, v, o, lse, B, L, n_q, n_kv, d_h, causal, scale);
+  if (bad != ATTN_OK) return bad;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  DeviceState* st = nullptr;
+  const attn_status_t ds = device_state(stream, &st);
+  if (ds != ATTN_OK) return ds;
+
+  int T = 0, units = 0;
+  count_units(B, L, n_q, n_kv, &T, &units);
+  CUtensorMap mq, mk, mv;
+  if (!encode_bhld(&mq, q, d_h, n_q, L, B) || !encode_bhld(&mk, k, d_h, n_kv, L, B) ||
+      !encode_bhld(&mv, v, d_h, n_kv, L, B))
+    return ATTN_ERR_CUDA;
+
+  Params p;
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  p.status = st->status;
+  p.L = static_cast<int>(L);
+  p.n_q = n_q;
+  p.n_kv = n_kv;
+  p.g = n_q / n_kv;
+  p.T = T;
+  p.causal = causal;
+  p.c = scale * 1.4426950408889634f;
+  p.scale_pos = p.c > 0.0f ? 1 : 0;
+  p.groups = static_cast<int>(B * n_kv);
+  p.units = units;
+  p.spin_limit = kSpinLimitCycles;
+
+  const int grid = units < st->sms ? units : st->sms;
+  if (d_h == 128)
+    attn_prefill_fwd_kernel<128><<<grid, kThreads, Tile<128>::kSmemBytes, stream>>>(mq, mk, mv, p);
+  else
+    attn_prefill_fwd_kernel<64><<<grid, kThreads, Tile<64>::kSmemBytes, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+const char* attn_status_string(attn_status_t status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG: invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED: unsupported size, head dim or device";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: CUDA call or kernel launch failed";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a device-side wait exceeded its limit";
+  }
+  return "ATTN_ERR_UNKNOWN";
+}
+
+attn_status_t attn_device_check(void* stream_ptr) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  int* status = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_dev[dev].ready) return ATTN_OK;
+    status = g_dev[dev].status;
+  }
+  int word = 0;
+  if (cudaMemcpy(&word, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (word == 0) return ATTN_OK;
+  if (cudaMemset(status, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_ERR_TIMEOUT;
+}
+
+int64_t attn_prefill_grid_size(int64_t B, int64_t L, int32_t n_q, int32_t n_kv, int32_t d_h,
+                               int32_t causal) {
+  if (B < 1 || L < 1 || n_q < 1 || n_kv < 1 || n_q % n_kv != 0 || (causal != 0 && causal != 1) ||
+      (d_h != 64 && d_h != 128))
+    return -1;
+  int T = 0, units = 0;
+  if (!count_units(B, L, n_q, n_kv, &T, &units)) return -1;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return -1;
+  return units < sms ? units : sms;
+}
+
+}  // extern "C"

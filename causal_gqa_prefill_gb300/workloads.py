@@ -1,0 +1,116 @@
+"""Seeded synthetic workloads shaped like the pages' models (no attention math here).
+
+Both the CUDA path's tests/benchmark and the oracle's checks draw their inputs
+from this module; it holds only shapes, seeds, random draws and the
+sampled-row selector.
+
+Recipe: seed = 1000 + config number; a torch.Generator on the target device
+draws Q, K, V in that order as float32 N(0, 1), each rounded to bf16 (round to
+nearest even). The 70B-shaped workload multiplies K channels 0..3 of every
+K/V head by 8 (N(0, 8^2) there), which pushes single logits far above the
+rest and exercises the online-softmax rescaling.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+
+@dataclass(frozen=True)
+class Workload:
+    number: int
+    name: str
+    B: int
+    L: int
+    n_q: int
+    n_kv: int
+    d_h: int
+    causal: bool = True
+    heavy_k_channels: int = 0       # leading K channels drawn with std 8
+    full_check: bool = True         # oracle over every row (else sampled rows)
+
+    @property
+    def g(self) -> int:
+        return self.n_q // self.n_kv
+
+    @property
+    def seed(self) -> int:
+        return 1000 + self.number
+
+    @property
+    def scale(self) -> float:
+        return self.d_h ** -0.5
+
+    def metric_flops(self) -> int:
+        """Causal prefill FLOPs as the metric counts them: 2*n_q*d_h*L^2*B."""
+        f = 2 * self.n_q * self.d_h * self.L * self.L * self.B
+        return f if self.causal else 2 * f
+
+    def io_bytes(self) -> int:
+        """Bytes read and written once: Q, K, V, O in bf16 and LSE in fp32."""
+        e = self.B * self.L * self.d_h * 2
+        return e * (2 * self.n_q + 2 * self.n_kv) + self.B * self.n_q * self.L * 4
+
+    def describe(self) -> dict:
+        return {"workload": self.name, "B": self.B, "L": self.L, "n_q": self.n_q,
+                "n_kv": self.n_kv, "d_h": self.d_h, "causal": self.causal}
+
+
+WORKLOADS = {
+    1: Workload(1, "tiny GQA-4 (B=1, L=256, n_q=4, n_kv=1, d_h=64)", 1, 256, 4, 1, 64),
+    2: Workload(2, "Llama-2-7B-shaped layer, MHA (B=4, L=2048, n_q=n_kv=32, d_h=128)",
+                4, 2048, 32, 32, 128),
+    3: Workload(3, "Llama-3-8B-shaped layer, GQA-4 (B=1, L=8192, n_q=32, n_kv=8, d_h=128)",
+                1, 8192, 32, 8, 128),
+    4: Workload(4, "Llama-2-70B-shaped layer, GQA-8, heavy K channels "
+                   "(B=1, L=32768, n_q=64, n_kv=8, d_h=128)",
+                1, 32768, 64, 8, 128, heavy_k_channels=4, full_check=False),
+    5: Workload(5, "long-context 36-head shape, GQA-6 (B=1, L=131072, n_q=36, n_kv=6, d_h=128)",
+                1, 131072, 36, 6, 128, full_check=False),
+}
+
+
+def make_inputs(w: Workload, device="cuda", seed: int | None = None):
+    """Seeded bf16 (q, k, v) for workload ``w`` on ``device``."""
+    import torch
+
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed if seed is None else seed)
+    shape_q = (w.B, w.L, w.n_q, w.d_h)
+    shape_kv = (w.B, w.L, w.n_kv, w.d_h)
+    q = torch.randn(shape_q, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+    k = torch.randn(shape_kv, generator=gen, device=device, dtype=torch.float32)
+    if w.heavy_k_channels:
+        k[..., :w.heavy_k_channels] *= 8.0
+    k = k.to(torch.bfloat16)
+    v = torch.randn(shape_kv, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+    return q, k, v
+
+
+def custom(B, L, n_q, n_kv, d_h, causal=True, number=0, name=None) -> Workload:
+    return Workload(number, name or f"B={B} L={L} n_q={n_q} n_kv={n_kv} d_h={d_h}",
+                    B, L, n_q, n_kv, d_h, causal)
+
+
+def sampled_rows(w: Workload, count: int = 4096, tile: int = 128):
+    """Rows (b, h, i) to check on large workloads.
+
+    For s = 0..count-1: position in tile = s mod 128 and head =
+    (s + s div 128) mod n_q, so every head and every intra-tile position is
+    covered and heads meet many positions; query tile and batch index are
+    drawn from numpy's default_rng(seed) uniformly. Rows 0 and L-1 of every
+    (b, head) are added. Returns a sorted, de-duplicated int64 array [R, 3].
+    """
+    import numpy as np
+
+    T = (w.L + tile - 1) // tile
+    rng = np.random.default_rng(w.seed)
+    s = np.arange(count, dtype=np.int64)
+    i = rng.integers(0, T, count) * tile + (s % tile)
+    i = np.minimum(i, w.L - 1)
+    b = rng.integers(0, w.B, count)
+    rows = [np.stack([b, (s + s // tile) % w.n_q, i], axis=1)]
+    for bb in range(w.B):
+        for h in range(w.n_q):
+            rows.append(np.array([[bb, h, 0], [bb, h, w.L - 1]], dtype=np.int64))
+    return np.unique(np.concatenate(rows, axis=0), axis=0)

@@ -1,0 +1,108 @@
+/*
+ * attn_prefill.h — C ABI of the GB300 (sm_103a) causal GQA prefill attention
+ * forward pass.
+ *
+ * Operation (one call computes, for every batch b, query head h and row i):
+ *
+ *     kv(h)       = h / g,  g = n_q / n_kv            (contiguous head groups)
+ *     s_ij        = scale * dot(Q[b,i,h,:], K[b,j,kv(h),:])
+ *     J(i)        = {0..i} if causal, else {0..L-1}    (diagonal kept)
+ *     O[b,i,h,:]  = sum_{j in J(i)} softmax_j(s_i.) * V[b,j,kv(h),:]
+ *     LSE[b,h,i]  = ln sum_{j in J(i)} exp(s_ij)
+ *
+ * as defined by "Why Attention Scaling Breaks" (shivam2003), section
+ * "The O(n^2) problem" (S = Q K^T, A = softmax(S / sqrt(d)), O = A V), with
+ * the causal restriction of "Long-Context Attention Explained" (sevydevy),
+ * quadratic-cost section (each token looks only backwards, itself included),
+ * and the grouped K/V heads of the "prefill-attention" flop record
+ * (phantomic12), "Workarounds" (MQA/GQA). It is evaluated the FlashAttention
+ * way, tile by tile with an online softmax ("Long-Context Attention
+ * Explained", sections "Tiling" and "Online softmax"), so the L x L score
+ * matrix never reaches device memory.
+ *
+ * Layouts (all row-major, contiguous, device memory):
+ *     q   bf16 [B, L, n_q,  d_h]
+ *     k   bf16 [B, L, n_kv, d_h]
+ *     v   bf16 [B, L, n_kv, d_h]
+ *     o   bf16 [B, L, n_q,  d_h]   written
+ *     lse fp32 [B, n_q, L]         written (natural log, of the scaled scores)
+ *
+ * Ownership: the caller allocates and owns q, k, v, o, lse and the stream.
+ * The library never frees caller memory and allocates nothing per call. On
+ * the first call on a device it allocates one 256-byte status word for that
+ * device (kept until process exit) and sets the kernels' shared-memory limit.
+ *
+ * Execution: asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ * stream). The call returns after the launch is enqueued; o and lse are valid
+ * once the stream has reached that point. q, k, v are not modified. Results
+ * are deterministic: the same inputs give bit-identical o and lse.
+ */
+#ifndef ATTN_PREFILL_H
+#define ATTN_PREFILL_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,  /* NULL pointer, non-positive size, n_q % n_kv != 0,
+                                non-finite scale, causal not 0/1, misaligned pointer */
+  ATTN_ERR_UNSUPPORTED = 2,  /* d_h not 64 or 128, sizes beyond 32-bit tile indexing,
+                                device that is not sm_103 */
+  ATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call or the launch failed */
+  ATTN_ERR_TIMEOUT = 4       /* a kernel wait ran past its limit (reported by
+                                attn_device_check); outputs of that launch are
+                                undefined */
+} attn_status_t;
+
+/*
+ * Causal (or full) GQA attention forward over bf16 [B, L, H, d_h] tensors.
+ *
+ *   q, k, v   device pointers, 16-byte aligned, layouts above
+ *   o         device pointer, 16-byte aligned, bf16 [B, L, n_q, d_h]
+ *   lse       device pointer, 4-byte aligned, fp32 [B, n_q, L]; never NULL
+ *   B, L      batch size and sequence length, >= 1
+ *   n_q, n_kv query heads and K/V heads, >= 1, n_q a multiple of n_kv
+ *   d_h       head dimension: 64 or 128
+ *   causal    1: key j <= query i is kept (diagonal included); 0: all keys
+ *   scale     finite multiplier of the dot products (1/sqrt(d_h) in the usual
+ *             case; 0 and negative values are allowed)
+ *   stream    cudaStream_t to enqueue on, passed as void*
+ *
+ * Returns ATTN_OK after enqueueing. Argument errors return synchronously
+ * before any CUDA call or launch. A device-side wait that runs past its
+ * limit is reported by attn_device_check().
+ */
+attn_status_t attn_prefill_fwd(const void* q, const void* k, const void* v,
+                               void* o, float* lse,
+                               int64_t B, int64_t L, int32_t n_q, int32_t n_kv,
+                               int32_t d_h, int32_t causal, float scale,
+                               void* stream);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* attn_status_string(attn_status_t status);
+
+/*
+ * Synchronises `stream`, then reports: ATTN_ERR_CUDA if the stream or an
+ * earlier launch failed, ATTN_ERR_TIMEOUT if any launch on the current device
+ * since the previous check hit a wait limit (the status word is then cleared),
+ * else ATTN_OK.
+ */
+attn_status_t attn_device_check(void* stream);
+
+/*
+ * Number of persistent CTAs the forward kernel launches for these sizes on
+ * the current device (min(#SMs, #work units)), or -1 on an argument error.
+ * Host-side only apart from the SM-count query; used for reporting.
+ */
+int64_t attn_prefill_grid_size(int64_t B, int64_t L, int32_t n_q, int32_t n_kv,
+                               int32_t d_h, int32_t causal);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_PREFILL_H */

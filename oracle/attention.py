@@ -91,18 +91,32 @@ def _rows_block(qrows, krows, vrows, row_idx, causal, scale):
     return o, lse
 
 
-def attention_rows(q, k, v, rows, *, causal: bool = True, scale: float | None = None):
+def attention_rows(q, k, v, rows, *, causal: bool = True, scale: float | None = None,
+                   n_q: int | None = None):
     """Attention output for selected query rows only.
 
-    q: [B, L, n_q, d] (only the rows named in ``rows`` are read), k, v:
-    [B, L, n_kv, d]. ``rows``: integer array [R, 3] of (b, h, i).
+    ``rows``: integer array [R, 3] of (b, h, i). ``q`` is either the full
+    [B, L, n_q, d] query tensor or just the R query vectors [R, d] of the
+    listed rows, in the order of ``rows`` (then ``n_q`` must be given).
+    k, v: [B, L, n_kv, d].
     Returns (o [R, d] float64, lse [R] float64) in the order of ``rows``.
     """
-    B, L, n_q, n_kv, d = _check_shapes(q, k, v)
+    rows = np.asarray(rows, dtype=np.int64).reshape(-1, 3)
+    if q.ndim == 4:
+        B, L, n_q, n_kv, d = _check_shapes(q, k, v)
+        q_vec = None
+    else:
+        if n_q is None:
+            raise ValueError("n_q is required when q holds only the selected rows")
+        if q.ndim != 2 or q.shape[0] != rows.shape[0] or k.ndim != 4 or k.shape != v.shape:
+            raise ValueError("q must be [R, d] matching rows; k, v [B, L, n_kv, d]")
+        B, L, n_kv, d = k.shape
+        if q.shape[1] != d or n_q % n_kv:
+            raise ValueError("head dim mismatch or n_q not a multiple of n_kv")
+        q_vec = q
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     scale = float(scale)
-    rows = np.asarray(rows, dtype=np.int64).reshape(-1, 3)
     if rows.size and (rows.min(axis=0) < 0).any():
         raise ValueError("negative row index")
     if rows.size and ((rows[:, 0] >= B).any() or (rows[:, 1] >= n_q).any() or (rows[:, 2] >= L).any()):
@@ -125,10 +139,13 @@ def attention_rows(q, k, v, rows, *, causal: bool = True, scale: float | None = 
         step = max(1, min(256, _MAX_SCORE_ELEMS // max(L, 1)))
         for s0 in range(0, idx.size, step):
             sel = idx[s0:s0 + step]
-            lk = int(sel.max()) + 1 if causal else L
-            qrows = np.asarray(q[b, sel, h, :], dtype=np.float64)
-            o, lse = _rows_block(qrows, kmat[:lk], vmat[:lk], sel, causal, scale)
             dest = order[grp[s0:s0 + step]]
+            lk = int(sel.max()) + 1 if causal else L
+            if q_vec is None:
+                qrows = np.asarray(q[b, sel, h, :], dtype=np.float64)
+            else:
+                qrows = np.asarray(q_vec[dest], dtype=np.float64)
+            o, lse = _rows_block(qrows, kmat[:lk], vmat[:lk], sel, causal, scale)
             out_o[dest] = o
             out_lse[dest] = lse
     return out_o, out_lse

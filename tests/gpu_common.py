@@ -1,0 +1,63 @@
+"""Shared helpers for the GPU parity tests: run the CUDA path, run the oracle on
+the same bf16 inputs, compare with the acceptance tolerances.
+
+Acceptance (bf16 O and fp32 LSE against the fp64 oracle):
+  * O: max |err| <= 1e-2 and ||err||_F / ||O_ref||_F <= 5e-3
+  * LSE: max |err| <= 1e-3
+"""
+
+import numpy as np
+
+import oracle
+from causal_gqa_prefill_gb300 import attn_prefill, attn_device_check, ATTN_OK
+
+O_MAX_ABS = 1e-2
+O_REL_FRO = 5e-3
+LSE_MAX_ABS = 1e-3
+
+
+def to_np(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def run_gpu(q, k, v, causal=True, scale=None):
+    o, lse = attn_prefill(q, k, v, causal=causal, scale=scale)
+    st = attn_device_check()
+    assert st == ATTN_OK, f"device check returned {st}"
+    return o, lse
+
+
+def errors(o_gpu, lse_gpu, o_ref, lse_ref):
+    d = o_gpu - o_ref
+    fro = np.linalg.norm(d) / max(np.linalg.norm(o_ref), 1e-30)
+    return {"o_max_abs": float(np.abs(d).max()) if d.size else 0.0, "o_rel_fro": float(fro),
+            "lse_max_abs": float(np.abs(lse_gpu - lse_ref).max()) if lse_ref.size else 0.0}
+
+
+def assert_within(err, what=""):
+    assert np.isfinite(err["o_max_abs"]) and np.isfinite(err["lse_max_abs"]), (what, err)
+    assert err["o_max_abs"] <= O_MAX_ABS, (what, err)
+    assert err["o_rel_fro"] <= O_REL_FRO, (what, err)
+    assert err["lse_max_abs"] <= LSE_MAX_ABS, (what, err)
+
+
+def check_full(q, k, v, o, lse, causal=True, scale=None, what=""):
+    o_ref, lse_ref = oracle.attention(to_np(q), to_np(k), to_np(v), causal=causal, scale=scale)
+    err = errors(to_np(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref)
+    assert_within(err, what)
+    return err
+
+
+def check_rows(q, k, v, o, lse, rows, causal=True, scale=None, what=""):
+    import torch
+
+    n_q = q.shape[2]
+    r = torch.as_tensor(rows, device=q.device)
+    q_sel = to_np(q[r[:, 0], r[:, 2], r[:, 1]])
+    o_sel = to_np(o[r[:, 0], r[:, 2], r[:, 1]])
+    lse_sel = lse[r[:, 0], r[:, 1], r[:, 2]].cpu().numpy().astype(np.float64)
+    o_ref, lse_ref = oracle.attention_rows(q_sel, to_np(k), to_np(v), rows, causal=causal,
+                                           scale=scale, n_q=n_q)
+    err = errors(o_sel, lse_sel, o_ref, lse_ref)
+    assert_within(err, what)
+    return err

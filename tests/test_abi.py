@@ -1,0 +1,117 @@
+"""Host-side checks of the C ABI (no GPU needed, no compute call).
+
+The library is built here if needed (nvcc cross-compiles sm_103a without a
+GPU), loaded, and checked to export every function the public header
+declares. Argument validation is exercised only with calls that the library
+rejects before its first CUDA call.
+"""
+
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+import causal_gqa_prefill_gb300 as cg
+from causal_gqa_prefill_gb300 import build, workloads
+from oracle import flops as oflops
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return cg.load_library()
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(attn_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("attn_prefill_fwd", "attn_status_string", "attn_device_check"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        s = cg.status_string(code)
+        assert s.startswith("ATTN_")
+    assert "UNKNOWN" in cg.status_string(99)
+
+
+FAKE = 1 << 20   # 16-byte aligned, never dereferenced: each call fails validation first
+
+
+@pytest.mark.parametrize("args,expect", [
+    (dict(q=0), cg.ATTN_ERR_INVALID_ARG),
+    (dict(lse=0), cg.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), cg.ATTN_ERR_INVALID_ARG),
+    (dict(L=0), cg.ATTN_ERR_INVALID_ARG),
+    (dict(L=-5), cg.ATTN_ERR_INVALID_ARG),
+    (dict(n_q=6, n_kv=4), cg.ATTN_ERR_INVALID_ARG),
+    (dict(n_kv=0), cg.ATTN_ERR_INVALID_ARG),
+    (dict(causal=2), cg.ATTN_ERR_INVALID_ARG),
+    (dict(scale=math.nan), cg.ATTN_ERR_INVALID_ARG),
+    (dict(scale=math.inf), cg.ATTN_ERR_INVALID_ARG),
+    (dict(q=FAKE + 8), cg.ATTN_ERR_INVALID_ARG),
+    (dict(o=FAKE + 2), cg.ATTN_ERR_INVALID_ARG),
+    (dict(lse=FAKE + 2), cg.ATTN_ERR_INVALID_ARG),
+    (dict(d_h=96), cg.ATTN_ERR_UNSUPPORTED),
+    (dict(d_h=256), cg.ATTN_ERR_UNSUPPORTED),
+    (dict(L=1 << 31), cg.ATTN_ERR_UNSUPPORTED),
+])
+def test_validation_rejects_before_any_cuda_call(lib, args, expect):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, L=128, n_q=4, n_kv=2, d_h=128,
+             causal=1, scale=0.125)
+    a.update(args)
+    st = cg.attn_prefill_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["L"], a["n_q"],
+                             a["n_kv"], a["d_h"], a["causal"], a["scale"], stream=0)
+    assert st == expect
+
+
+def test_grid_size_argument_errors(lib):
+    assert cg.attn_prefill_grid_size(0, 128, 4, 2, 128) == -1
+    assert cg.attn_prefill_grid_size(1, 128, 4, 3, 128) == -1
+    assert cg.attn_prefill_grid_size(1, 128, 4, 2, 80) == -1
+
+
+def test_wrapper_rejects_host_tensors():
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        cg.attn_prefill(x, x, x)
+
+
+def test_metric_flops_match_the_oracle_cost_model():
+    for w in workloads.WORKLOADS.values():
+        assert w.metric_flops() == oflops.causal_attention_flops(w.B, w.L, w.n_q, w.d_h)
+
+
+def test_sampled_rows_cover_heads_and_tile_positions():
+    for w in (workloads.WORKLOADS[4], workloads.WORKLOADS[5]):
+        rows = workloads.sampled_rows(w)
+        assert rows.shape[1] == 3 and len(rows) >= 4000
+        assert set(rows[:, 1]) == set(range(w.n_q))
+        assert set(rows[:, 2] % 128) == set(range(128))
+        for h in range(w.n_q):
+            sel = rows[rows[:, 1] == h, 2]
+            assert 0 in sel and w.L - 1 in sel
+        assert (rows[:, 2] < w.L).all() and (rows[:, 2] >= 0).all()
+        T = w.L // 128
+        assert len(set(rows[:, 2] // 128)) >= min(T, 200)
