@@ -4,6 +4,15 @@ the same bf16 inputs, compare with the acceptance tolerances.
 Acceptance (bf16 O and fp32 LSE against the fp64 oracle):
   * O: max |err| <= 1e-2 and ||err||_F / ||O_ref||_F <= 5e-3
   * LSE: max |err| <= 1e-3
+
+The flat 1e-2 bound on O holds for the model-shaped workloads (soft softmax,
+|O| below ~2.5). Stress inputs that make the softmax nearly one-hot (large
+scale, keys x40) drive |O| to |V| (~4.5), where bf16 cannot represent the
+exact answer within 1e-2: its spacing on [4, 8) is 2^-5, so rounding the
+exact result alone can cost 2^-6 = 0.0156. For those cases the element bound
+is 1e-2 + 2^-8 |O_ref|: the bf16 rounding of O (<= 2^-8 |O| relative) on top
+of the flat bound, which already covers the bf16 rounding of P (<= 2^-8 per
+weight). Frobenius and LSE bounds are unchanged.
 """
 
 import numpy as np
@@ -30,21 +39,26 @@ def run_gpu(q, k, v, causal=True, scale=None):
 def errors(o_gpu, lse_gpu, o_ref, lse_ref):
     d = o_gpu - o_ref
     fro = np.linalg.norm(d) / max(np.linalg.norm(o_ref), 1e-30)
+    scaled = np.abs(d) - 2.0 ** -8 * np.abs(o_ref)
     return {"o_max_abs": float(np.abs(d).max()) if d.size else 0.0, "o_rel_fro": float(fro),
+            "o_max_abs_less_bf16_rounding": float(scaled.max()) if d.size else 0.0,
             "lse_max_abs": float(np.abs(lse_gpu - lse_ref).max()) if lse_ref.size else 0.0}
 
 
-def assert_within(err, what=""):
+def assert_within(err, what="", stress=False):
     assert np.isfinite(err["o_max_abs"]) and np.isfinite(err["lse_max_abs"]), (what, err)
-    assert err["o_max_abs"] <= O_MAX_ABS, (what, err)
+    if stress:
+        assert err["o_max_abs_less_bf16_rounding"] <= O_MAX_ABS, (what, err)
+    else:
+        assert err["o_max_abs"] <= O_MAX_ABS, (what, err)
     assert err["o_rel_fro"] <= O_REL_FRO, (what, err)
     assert err["lse_max_abs"] <= LSE_MAX_ABS, (what, err)
 
 
-def check_full(q, k, v, o, lse, causal=True, scale=None, what=""):
+def check_full(q, k, v, o, lse, causal=True, scale=None, what="", stress=False):
     o_ref, lse_ref = oracle.attention(to_np(q), to_np(k), to_np(v), causal=causal, scale=scale)
     err = errors(to_np(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref)
-    assert_within(err, what)
+    assert_within(err, what, stress)
     return err
 
 
