@@ -151,7 +151,7 @@ def kernel_source_hash() -> str:
 def recorded_traffic(workload_number: int):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.tsv")
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
     src = kernel_source_hash()
