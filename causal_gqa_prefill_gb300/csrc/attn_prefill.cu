@@ -691,3 +691,119 @@ int64_t attn_prefill_grid_size(int64_t B, int64_t L, int32_t n_q, int32_t n_kv, 
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------- allocation-free variant
+//
+// For callers that cannot allocate device memory: code running inside a
+// memory pool or arena that must own every allocation (a cudaMalloc behind
+// its back escapes its accounting and limits), or a host framework that
+// forbids the library from touching the allocator. The only global memory the kernel
+// needs beyond its inputs and outputs is its status word; here that word
+// lives in the fixed array below, part of the library's own device image.
+
+constexpr size_t kNoAllocScratchBytes = 256;       // stated maximum scratch
+constexpr size_t kNoAllocScratchNeeded = sizeof(int);   // one status word, any problem size
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+struct NoAllocState {
+  bool ready = false;
+  int sms = 0;
+  int* scratch = nullptr;    // device address of g_noalloc_scratch on this device
+};
+
+NoAllocState g_noalloc[kMaxDevices];
+
+// Once per device, with that device current: resolve the device address of
+// the static scratch array (the host-side symbol is only a stand-in and must
+// never be handed to a kernel), query the device, set the kernels'
+// shared-memory limit and resolve the tensor-map encoder. Nothing here
+// allocates.
+attn_status_t noalloc_state(NoAllocState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  NoAllocState& st = g_noalloc[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;
+    if (!g_encode) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return ATTN_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    if (cudaFuncSetAttribute(attn_prefill_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Tile<64>::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_prefill_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Tile<128>::kSmemBytes) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    void* scratch = nullptr;
+    if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || scratch == nullptr)
+      return ATTN_ERR_CUDA;
+    st.sms = sms;
+    st.scratch = static_cast<int*>(scratch);
+    st.ready = true;
+  }
+  *out = &st;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" attn_status_t attn_prefill_fwd_noalloc(const void* q, const void* k, const void* v,
+                                                  void* o, float* lse, int64_t B, int64_t L,
+                                                  int32_t n_q, int32_t n_kv, int32_t d_h,
+                                                  int32_t causal, float scale, void* stream_ptr) {
+  const attn_status_t bad = validate(q, k, v, o, lse, B, L, n_q, n_kv, d_h, causal, scale);
+  if (bad != ATTN_OK) return bad;
+  if (kNoAllocScratchNeeded > kNoAllocScratchBytes) return ATTN_ERR_UNSUPPORTED;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  NoAllocState* st = nullptr;
+  const attn_status_t ds = noalloc_state(&st);
+  if (ds != ATTN_OK) return ds;
+
+  int T = 0, units = 0;
+  count_units(B, L, n_q, n_kv, &T, &units);
+  CUtensorMap mq, mk, mv;
+  if (!encode_bhld(&mq, q, d_h, n_q, L, B) || !encode_bhld(&mk, k, d_h, n_kv, L, B) ||
+      !encode_bhld(&mv, v, d_h, n_kv, L, B))
+    return ATTN_ERR_CUDA;
+  // The status word must start at zero for every call (the kernel only ORs
+  // error bits into it).
+  if (cudaMemsetAsync(st->scratch, 0, kNoAllocScratchNeeded, stream) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+
+  Params p;
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  p.status = st->scratch;
+  p.L = static_cast<int>(L);
+  p.n_q = n_q;
+  p.n_kv = n_kv;
+  p.g = n_q / n_kv;
+  p.T = T;
+  p.causal = causal;
+  p.c = scale * 1.4426950408889634f;
+  p.scale_pos = p.c > 0.0f ? 1 : 0;
+  p.groups = static_cast<int>(B * n_kv);
+  p.units = units;
+  p.spin_limit = kSpinLimitCycles;
+
+  const int grid = units < st->sms ? units : st->sms;
+  if (d_h == 128)
+    attn_prefill_fwd_kernel<128><<<grid, kThreads, Tile<128>::kSmemBytes, stream>>>(mq, mk, mv, p);
+  else
+    attn_prefill_fwd_kernel<64><<<grid, kThreads, Tile<64>::kSmemBytes, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}

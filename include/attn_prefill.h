@@ -101,6 +101,37 @@ attn_status_t attn_device_check(void* stream);
 int64_t attn_prefill_grid_size(int64_t B, int64_t L, int32_t n_q, int32_t n_kv,
                                int32_t d_h, int32_t causal);
 
+/*
+ * Allocation-free variant of attn_prefill_fwd. (No counterpart on the pages:
+ * this is a deployment convenience of this library.)
+ *
+ * Same arguments, layouts, results and errors as attn_prefill_fwd, for
+ * callers that cannot let a library allocate device memory: code whose
+ * device memory all comes from its own pool or arena (a cudaMalloc behind
+ * its back would escape its accounting and limits), or a host framework
+ * that owns the allocator and forbids libraries to call it. The one piece of global scratch the kernel uses
+ * (its 4-byte status word) sits in a fixed 256-byte array compiled into the
+ * library instead of a cudaMalloc'd buffer; every GPU that loads the library
+ * holds that array until process exit. This kernel's scratch does not grow
+ * with the problem size, so every size attn_prefill_fwd accepts fits; a
+ * build whose scratch exceeded the 256 bytes would return
+ * ATTN_ERR_UNSUPPORTED.
+ *
+ * The first call on a device does a one-time set-up on that device (it
+ * looks up the array's device address and sets the kernels' shared-memory
+ * limit, without allocating); make that first call before any stream capture.
+ * Each call clears the status word on `stream` before its launch. All calls
+ * share the one array: calls that overlap on the GPU (different streams, no
+ * ordering between them) race on it. A wait that runs past its limit in this
+ * variant is recorded only in that array; attn_device_check does not report
+ * it.
+ */
+attn_status_t attn_prefill_fwd_noalloc(const void* q, const void* k, const void* v,
+                                       void* o, float* lse,
+                                       int64_t B, int64_t L, int32_t n_q, int32_t n_kv,
+                                       int32_t d_h, int32_t causal, float scale,
+                                       void* stream);
+
 #ifdef __cplusplus
 }
 #endif
