@@ -79,9 +79,14 @@ class Dist:
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Only samples whose timestamp falls inside the timed window are summarised;
+    if the window is too short to catch one, the samples of the warm-up plus
+    the timed window are used and the summary says so.
+    """
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -89,6 +94,8 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.t_start = None
+        self.window = None
 
     def start(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -101,8 +108,14 @@ class ClockSampler:
         except OSError:
             self.proc = None
         time.sleep(0.3)
+        self.t_start = time.time()
+
+    def mark_window(self, t0: float, t1: float):
+        self.window = (t0, t1)
 
     def stop(self) -> dict:
+        import datetime
+
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         time.sleep(0.25)
@@ -115,23 +128,28 @@ class ClockSampler:
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[2]), float(parts[3]), float(parts[4]), parts[6:10]))
                 except ValueError:
                     continue
         os.remove(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        peak_power = max(r[2] for r in rows)
-        loaded = [r for r in rows if r[2] >= 0.5 * peak_power] or rows
+        span = "timed"
+        sel = [r for r in rows if self.window and self.window[0] <= r[0] <= self.window[1]]
+        if not sel:
+            span = "warm-up + timed (timed window shorter than the 100 ms sampling period)"
+            lo = self.t_start if self.t_start else rows[0][0]
+            hi = self.window[1] if self.window else rows[-1][0]
+            sel = [r for r in rows if lo <= r[0] <= hi] or rows
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3])
-                          if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded),
-                "power_w_max": peak_power}
+        reasons = sorted({names[i] for r in sel for i, v in enumerate(r[4]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": max(r[2] for r in rows),
+                "reasons": reasons, "samples": len(sel), "window": span,
+                "power_w_median": statistics.median(r[3] for r in sel)}
 
 
 def measured_peaks():
@@ -225,7 +243,12 @@ def run_reference(args, w, dist):
         return 0
     q, k, v = host_inputs(w)
     rng = np.random.default_rng(w.seed)
-    rows_per_step = args.ref_rows
+    # Size each step so that warm-up plus timed steps take about
+    # --ref-seconds of oracle time in total (calibrated on one chunk).
+    f, s, n = oracle_sample(w, q, k, v, rng, 64, chunks=1)
+    per_row = s / n
+    budget = args.ref_seconds / (args.steps + args.warmup)
+    rows_per_step = int(min(args.ref_rows, max(8, budget / max(per_row, 1e-9))))
     for _ in range(args.warmup):
         oracle_sample(w, q, k, v, rng, rows_per_step, chunks=1)
     total_flops, total_s = 0.0, 0.0
@@ -288,6 +311,7 @@ def run_ours(args, w, dist):
     dist.barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
+    t_epoch0 = time.time()
     for s, e in events:
         flush.zero_()
         s.record(stream)
@@ -296,6 +320,7 @@ def run_ours(args, w, dist):
     torch.cuda.synchronize()
     dist.barrier()
     t_wall = time.perf_counter() - t_wall
+    sampler.mark_window(t_epoch0, time.time())
     clocks = sampler.stop()
     st = cg.attn_device_check(sh)
     if st != cg.ATTN_OK:
@@ -375,12 +400,14 @@ def run_ours(args, w, dist):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--ref-rows", type=int, default=512)
+    ap.add_argument("--ref-rows", type=int, default=4096, help="upper bound on rows per step")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="oracle time budget of the whole reference run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -15,11 +15,15 @@
 // Attention Explained", FlashAttention-2 paragraph on causal block skipping),
 // and units are handed out longest first over a persistent grid.
 //
-// Warp roles (320 threads):
-//   warps 0-3  softmax for query tile 0     (thread = tile row = TMEM lane)
-//   warps 4-7  softmax for query tile 1
-//   warp  8    TMA producer (Q tiles, K/V ring)
-//   warp  9    tcgen05 MMA issuer; owns the TMEM allocation
+// Warp roles (384 threads, three warpgroups):
+//   warps 0-3   softmax for query tile 0    (thread = tile row = TMEM lane)
+//   warps 4-7   softmax for query tile 1
+//   warp  8     TMA producer (Q tiles, K/V ring)
+//   warp  9     tcgen05 MMA issuer; owns the TMEM allocation
+//   warps 10-11 idle
+// The softmax warpgroups raise their register limit to 224 and the third
+// warpgroup lowers its to 56 (setmaxnreg), so each softmax thread holds its
+// whole 128-score row in registers without spilling.
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0,128)   S0 scores, later P0 (bf16, packed two per column, cols 0..63)
 //   [128,256) S1 / P1
@@ -48,7 +52,13 @@ using namespace gb300;
 
 constexpr int kBM = 128;          // query rows per tile (= TMEM lanes)
 constexpr int kBN = 128;          // keys per K/V tile
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+constexpr int kSoftmaxRegs = 224;   // per thread, warpgroups 0 and 1
+constexpr int kOtherRegs = 56;      // per thread, warpgroup 2
+// The split must fit the registers the CTA is launched with (168 per thread
+// at 384 threads and one CTA per SM); the host checks the compiled count.
+constexpr int kRegBudget = 2 * 128 * kSoftmaxRegs + 128 * kOtherRegs;
+static_assert(kRegBudget <= kThreads * 168, "setmaxnreg split exceeds the launch allocation");
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
@@ -126,6 +136,15 @@ __device__ __forceinline__ Unit decode_unit(int u, const Params& p) {
   return x;
 }
 
+// Persistent schedule: round r of the grid takes units r*grid .. r*grid+grid-1
+// of the longest-first list, left to right on even rounds and right to left
+// on odd rounds (snake order), which balances the triangular causal work
+// without any shared counter.
+__device__ __forceinline__ int snake_unit(int r) {
+  const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return r * g + ((r & 1) ? (g - 1 - c) : c);
+}
+
 // Bounded wait: true when the phase completed; false if another role aborted
 // or this wait ran past the limit (then it raises the abort flag and the
 // device status word so the host sees ATTN_ERR_TIMEOUT).
@@ -163,9 +182,12 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
   uint32_t q_issued = 0;
   bool ok = true;
   int uc = 0;
-  for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++uc) {
+  for (int r = 0; r * static_cast<int>(gridDim.x) < p.units; ++r) {
+    const int u = snake_unit(r);
+    if (u >= p.units) continue;
     const Unit x = decode_unit(u, p);
     if (uc > 0 && !wait_phase(smem_addr(&ctl.q_empty), (uc - 1) & 1, ctl, p)) { ok = false; break; }
+    ++uc;
     const uint32_t qbar = smem_addr(&ctl.q_full);
     mbar_arrive_expect_tx(qbar, (x.n[0] > 0 ? 2u : 1u) * TL::kQBytes);
     ++q_issued;
@@ -240,9 +262,12 @@ __device__ void mma_role(Ctl& ctl, const Params& p, uint32_t tmem, uint32_t sQ0,
   uint32_t it = 0;
   uint32_t ph_p0 = 0, ph_p1 = 0;
   int uc = 0;
-  for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++uc) {
+  for (int r = 0; r * static_cast<int>(gridDim.x) < p.units; ++r) {
+    const int u = snake_unit(r);
+    if (u >= p.units) continue;
     const Unit x = decode_unit(u, p);
     if (!wait_phase(smem_addr(&ctl.q_full), uc & 1, ctl, p)) break;
+    ++uc;
     tc_fence_after_sync();
     uint32_t v_prev = 0;
     bool ok = true;
@@ -296,9 +321,22 @@ __device__ void mma_role(Ctl& ctl, const Params& p, uint32_t tmem, uint32_t sQ0,
 
 // ------------------------------------------------------------------- softmax
 
-__device__ __forceinline__ float fmax8(const float* v) {
-  return fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])),
-               fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Row maximum of 128 scores with three-input max instructions.
+__device__ __forceinline__ float row_max128(const float* v) {
+  float m[8];
+#pragma unroll
+  for (int t = 0; t < 8; ++t) m[t] = v[t];
+#pragma unroll
+  for (int i = 8; i < 128; i += 16)
+#pragma unroll
+    for (int t = 0; t < 8; ++t) m[t] = max3(m[t], v[i + t], v[i + 8 + t]);
+  return max3(max3(m[0], m[1], m[2]), max3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
 }
 
 template <int D>
@@ -312,36 +350,41 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem)
   const uint32_t bar_p = smem_addr(&ctl.p_full[slot]);
   const uint32_t bar_o = smem_addr(&ctl.o_done[slot]);
   const float cc = p.scale_pos ? p.c : 1.0f;
+  const uint64_t cc2 = f32x2_pack(cc, cc);
   uint32_t ph_s = 0, ph_o = 0;
 
-  for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+  for (int rr = 0; rr * static_cast<int>(gridDim.x) < p.units; ++rr) {
+    const int u = snake_unit(rr);
+    if (u >= p.units) continue;
     const Unit x = decode_unit(u, p);
     const int n = x.n[slot];
     if (n == 0) continue;
     const int row = x.qtile[slot] * kBM + r;
     float m_run = -INFINITY, l_run = 0.0f;
-    bool ok = true;
     for (int j = 0; j < n; ++j) {
-      if (!__all_sync(0xffffffffu, wait_phase(bar_s, ph_s, ctl, p))) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, wait_phase(bar_s, ph_s, ctl, p))) return;
       ph_s ^= 1;
       tc_fence_after_sync();
-      uint32_t sr[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
-      tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(sr));
-      tmem_after_wait(*reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-      tmem_after_wait(*reinterpret_cast<uint32_t(*)[32]>(sr + 64));
-      tmem_after_wait(*reinterpret_cast<uint32_t(*)[32]>(sr + 96));
       float s[128];
+      {
+        uint32_t* sr = reinterpret_cast<uint32_t*>(s);
 #pragma unroll
-      for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i]);
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
+        tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(sr));
+        tmem_after_wait(*reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+        tmem_after_wait(*reinterpret_cast<uint32_t(*)[32]>(sr + 64));
+        tmem_after_wait(*reinterpret_cast<uint32_t(*)[32]>(sr + 96));
+      }
       if (!p.scale_pos) {
+        // Non-positive scale: fold it in first so that masking and the
+        // maximum below work on the scaled scores (then cc = 1).
 #pragma unroll
         for (int i = 0; i < 128; ++i) s[i] *= p.c;
       }
       if (j == n - 1) {
         if (p.causal) {
-          // Diagonal tile: key index kBN*j + i against query kBM*qtile + r.
+          // Diagonal tile: key kBN*j + i against query kBM*qtile + r.
 #pragma unroll
           for (int i = 0; i < 128; ++i)
             if (i > r) s[i] = -INFINITY;
@@ -352,14 +395,7 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem)
             if (i >= lim) s[i] = -INFINITY;
         }
       }
-      float mx8[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) mx8[t] = s[t];
-#pragma unroll
-      for (int i = 8; i < 128; i += 8)
-#pragma unroll
-        for (int t = 0; t < 8; ++t) mx8[t] = fmaxf(mx8[t], s[i + t]);
-      const float m_tile = fmax8(mx8) * cc;
+      const float m_tile = row_max128(s) * cc;
       const float m_new = fmaxf(m_run, m_tile);
       const bool need = m_new > m_run + kRescaleThreshold;
       float alpha = 1.0f;
@@ -378,29 +414,35 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem)
           tmem_st32(tO + c, ov);
         }
       }
-      const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
       // P = 2^(c*s - m) as bf16 pairs into columns [0, 64) of this tile's S
-      // region (every score of the row is already in registers).
-      float sum0 = 0.0f, sum1 = 0.0f;
+      // region (every score of the row is already in registers). Two scores
+      // per packed FMA / add.
+      const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+      const uint64_t negm2 = f32x2_pack(-m_use, -m_use);
+      uint64_t sum2 = f32x2_pack(0.0f, 0.0f);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2_approx(fmaf(s[64 * h + 2 * i], cc, -m_use));
-          const float p1 = ex2_approx(fmaf(s[64 * h + 2 * i + 1], cc, -m_use));
-          sum0 += p0;
-          sum1 += p1;
+          const uint64_t xa = ffma2(f32x2_pack(s[64 * h + 2 * i], s[64 * h + 2 * i + 1]), cc2, negm2);
+          float x0, x1;
+          f32x2_unpack(xa, x0, x1);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          const uint64_t pp = f32x2_pack(p0, p1);
+          sum2 = fadd2(sum2, pp);
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st32(tS + 32 * h, pk);
       }
-      l_run = l_run * alpha + (sum0 + sum1);
+      float sa, sb;
+      f32x2_unpack(sum2, sa, sb);
+      l_run = l_run * alpha + (sa + sb);
       tmem_wait_st();
       tc_fence_before_sync();
       mbar_arrive(bar_p);
     }
-    if (!ok) return;
     // Epilogue: O = acc / l (bf16, round to nearest even) and LSE in natural log.
     if (!__all_sync(0xffffffffu, wait_phase(bar_o, ph_o, ctl, p))) return;
     ph_o ^= 1;
@@ -476,12 +518,16 @@ attn_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
   tc_fence_after_sync();
   const uint32_t tmem = ctl.tmem_base;
 
-  if (warp == kLoadWarp) {
-    if (lane == 0) load_role<D>(&tmQ, &tmK, &tmV, ctl, p, sQ0, sQ1, sKV);
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) mma_role<D>(ctl, p, tmem, sQ0, sQ1, sKV);
-  } else {
+  if (warp < 8) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     softmax_role<D>(warp >> 2, ctl, p, tmem);
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
+    if (warp == kLoadWarp) {
+      if (lane == 0) load_role<D>(&tmQ, &tmK, &tmV, ctl, p, sQ0, sQ1, sKV);
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) mma_role<D>(ctl, p, tmem, sQ0, sQ1, sKV);
+    }
   }
 
   tc_fence_before_sync();
@@ -510,6 +556,20 @@ std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
 EncodeTiledFn g_encode = nullptr;
 
+// The softmax warpgroups raise their register limit with setmaxnreg; that
+// only succeeds if the CTA was launched with at least kRegBudget registers,
+// so refuse to launch a build whose register count does not cover the split.
+bool kernel_registers_fit() {
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, attn_prefill_fwd_kernel<128>) != cudaSuccess ||
+      fa.numRegs * kThreads < kRegBudget)
+    return false;
+  if (cudaFuncGetAttributes(&fa, attn_prefill_fwd_kernel<64>) != cudaSuccess ||
+      fa.numRegs * kThreads < kRegBudget)
+    return false;
+  return true;
+}
+
 attn_status_t device_state(cudaStream_t stream, DeviceState** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
@@ -523,6 +583,7 @@ attn_status_t device_state(cudaStream_t stream, DeviceState** out) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return ATTN_ERR_CUDA;
     if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;   // built for sm_103a only
+    if (!kernel_registers_fit()) return ATTN_ERR_UNSUPPORTED;
     if (!g_encode) {
       cudaDriverEntryPointQueryResult q;
       void* fn = nullptr;
@@ -734,6 +795,7 @@ attn_status_t noalloc_state(NoAllocState** out) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return ATTN_ERR_CUDA;
     if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;
+    if (!kernel_registers_fit()) return ATTN_ERR_UNSUPPORTED;
     if (!g_encode) {
       cudaDriverEntryPointQueryResult q;
       void* fn = nullptr;
