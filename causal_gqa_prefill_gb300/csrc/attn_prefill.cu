@@ -19,7 +19,8 @@
 //   warps 0-3   softmax for query tile 0    (thread = tile row = TMEM lane)
 //   warps 4-7   softmax for query tile 1
 //   warp  8     TMA producer (Q tiles, K/V ring)
-//   warp  9     tcgen05 MMA issuer; owns the TMEM allocation
+//   warp  9     tcgen05 MMA issuer (the whole warp runs the loop warp-uniformly,
+//               one elected lane issues); owns the TMEM allocation
 //   warps 10-11 idle
 // The softmax warpgroups raise their register limit to 224 and the third
 // warpgroup lowers its to 56 (setmaxnreg), so each softmax thread holds its
@@ -171,6 +172,11 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
   }
 }
 
+// Bounded wait taken by a whole warp; the result is the same on every lane.
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, Ctl& ctl, const Params& p) {
+  return __all_sync(0xffffffffu, wait_phase(bar, parity, ctl, p));
+}
+
 // ------------------------------------------------------------------ producer
 
 template <int D>
@@ -178,6 +184,8 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                           const CUtensorMap* tmV, Ctl& ctl, const Params& p,
                           uint32_t sQ0, uint32_t sQ1, uint32_t sKV) {
   using TL = Tile<D>;
+  // Run by lane 0 alone: a whole warp polling the ring barriers would cost
+  // the softmax warps on this SM sub-partition more issue slots than it saves.
   uint32_t it = 0;       // K/V ring items issued
   uint32_t q_issued = 0;
   bool ok = true;
@@ -231,27 +239,29 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
 // ---------------------------------------------------------------- MMA issuer
 
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+__device__ __forceinline__ void issue_qk(bool leader, uint32_t d_tmem, uint32_t q_smem,
+                                         uint32_t k_smem) {
   constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     // K step kk: 16 bf16 = 32 bytes inside chunk kk/4 of the swizzled tile.
     const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-    mma_ss(d_tmem, sdesc_sw128(q_smem + off, 16, 1024), sdesc_sw128(k_smem + off, 16, 1024),
-           idesc, kk > 0 ? 1u : 0u);
+    const uint64_t a = sdesc_sw128(q_smem + off, 16, 1024);
+    const uint64_t b = sdesc_sw128(k_smem + off, 16, 1024);
+    if (leader) mma_ss(d_tmem, a, b, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
-                                         bool accumulate) {
+__device__ __forceinline__ void issue_pv(bool leader, uint32_t d_tmem, uint32_t p_tmem,
+                                         uint32_t v_smem, bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, true);
 #pragma unroll
   for (int kk = 0; kk < kBN / 16; ++kk) {
     // V tile is [keys][D] with D contiguous (MN-major for this product): 16
     // keys = 2048 bytes per K step; 64-column chunks are kBN*128 bytes apart.
     const uint64_t b = sdesc_sw128(v_smem + kk * 16 * 128, kBN * 128, 1024);
-    mma_ts(d_tmem, p_tmem + kk * 8, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
+    if (leader) mma_ts(d_tmem, p_tmem + kk * 8, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -259,6 +269,10 @@ template <int D>
 __device__ void mma_role(Ctl& ctl, const Params& p, uint32_t tmem, uint32_t sQ0, uint32_t sQ1,
                          uint32_t sKV) {
   using TL = Tile<D>;
+  // The whole warp runs this loop (so its control flow and descriptor math
+  // stay warp-uniform); one elected lane issues every tcgen05 instruction,
+  // which keeps all commits on the thread that issued the MMAs.
+  const bool leader = elect_one();
   uint32_t it = 0;
   uint32_t ph_p0 = 0, ph_p1 = 0;
   int uc = 0;
@@ -266,57 +280,58 @@ __device__ void mma_role(Ctl& ctl, const Params& p, uint32_t tmem, uint32_t sQ0,
     const int u = snake_unit(r);
     if (u >= p.units) continue;
     const Unit x = decode_unit(u, p);
-    if (!wait_phase(smem_addr(&ctl.q_full), uc & 1, ctl, p)) break;
+    if (!wait_all(smem_addr(&ctl.q_full), uc & 1, ctl, p)) break;
     ++uc;
     tc_fence_after_sync();
     uint32_t v_prev = 0;
     bool ok = true;
     for (int j = 0; j < x.nkv; ++j) {
       const uint32_t ks = it % TL::kStages;
-      if (!wait_phase(smem_addr(&ctl.kv_full[ks]), (it / TL::kStages) & 1, ctl, p)) { ok = false; break; }
+      if (!wait_all(smem_addr(&ctl.kv_full[ks]), (it / TL::kStages) & 1, ctl, p)) { ok = false; break; }
       ++it;
       tc_fence_after_sync();
       const uint32_t k_smem = sKV + ks * TL::kKVBytes;
       if (j < x.n[0]) {
-        issue_qk<D>(tmem + kColS0, sQ0, k_smem);
-        mma_commit(smem_addr(&ctl.s_full[0]));
+        issue_qk<D>(leader, tmem + kColS0, sQ0, k_smem);
+        if (leader) mma_commit(smem_addr(&ctl.s_full[0]));
       }
       if (j > 0) {
-        if (!wait_phase(smem_addr(&ctl.p_full[1]), ph_p1, ctl, p)) { ok = false; break; }
+        if (!wait_all(smem_addr(&ctl.p_full[1]), ph_p1, ctl, p)) { ok = false; break; }
         ph_p1 ^= 1;
         tc_fence_after_sync();
-        issue_pv<D>(tmem + kColO1, tmem + kColS1, sKV + v_prev * TL::kKVBytes, j - 1 > 0);
-        mma_commit(smem_addr(&ctl.kv_empty[v_prev]));
+        issue_pv<D>(leader, tmem + kColO1, tmem + kColS1, sKV + v_prev * TL::kKVBytes, j - 1 > 0);
+        if (leader) mma_commit(smem_addr(&ctl.kv_empty[v_prev]));
       }
-      issue_qk<D>(tmem + kColS1, sQ1, k_smem);
-      mma_commit(smem_addr(&ctl.s_full[1]));
-      mma_commit(smem_addr(&ctl.kv_empty[ks]));
-      if (j == x.nkv - 1) mma_commit(smem_addr(&ctl.q_empty));
+      issue_qk<D>(leader, tmem + kColS1, sQ1, k_smem);
+      if (leader) mma_commit(smem_addr(&ctl.s_full[1]));
+      if (leader) mma_commit(smem_addr(&ctl.kv_empty[ks]));
+      if (leader && j == x.nkv - 1) mma_commit(smem_addr(&ctl.q_empty));
 
       const uint32_t vs = it % TL::kStages;
-      if (!wait_phase(smem_addr(&ctl.kv_full[vs]), (it / TL::kStages) & 1, ctl, p)) { ok = false; break; }
+      if (!wait_all(smem_addr(&ctl.kv_full[vs]), (it / TL::kStages) & 1, ctl, p)) { ok = false; break; }
       ++it;
       tc_fence_after_sync();
       if (j < x.n[0]) {
-        if (!wait_phase(smem_addr(&ctl.p_full[0]), ph_p0, ctl, p)) { ok = false; break; }
+        if (!wait_all(smem_addr(&ctl.p_full[0]), ph_p0, ctl, p)) { ok = false; break; }
         ph_p0 ^= 1;
         tc_fence_after_sync();
-        issue_pv<D>(tmem + kColO0, tmem + kColS0, sKV + vs * TL::kKVBytes, j > 0);
-        if (j == x.n[0] - 1) mma_commit(smem_addr(&ctl.o_done[0]));
+        issue_pv<D>(leader, tmem + kColO0, tmem + kColS0, sKV + vs * TL::kKVBytes, j > 0);
+        if (leader && j == x.n[0] - 1) mma_commit(smem_addr(&ctl.o_done[0]));
       }
       v_prev = vs;
     }
     if (!ok) break;
-    if (!wait_phase(smem_addr(&ctl.p_full[1]), ph_p1, ctl, p)) break;
+    if (!wait_all(smem_addr(&ctl.p_full[1]), ph_p1, ctl, p)) break;
     ph_p1 ^= 1;
     tc_fence_after_sync();
-    issue_pv<D>(tmem + kColO1, tmem + kColS1, sKV + v_prev * TL::kKVBytes, x.nkv - 1 > 0);
-    mma_commit(smem_addr(&ctl.o_done[1]));
-    mma_commit(smem_addr(&ctl.kv_empty[v_prev]));
+    issue_pv<D>(leader, tmem + kColO1, tmem + kColS1, sKV + v_prev * TL::kKVBytes, x.nkv - 1 > 0);
+    if (leader) mma_commit(smem_addr(&ctl.o_done[1]));
+    if (leader) mma_commit(smem_addr(&ctl.kv_empty[v_prev]));
   }
   // No MMA may still be running when TMEM is released.
-  mma_commit(smem_addr(&ctl.drain));
+  if (leader) mma_commit(smem_addr(&ctl.drain));
   drain_wait(smem_addr(&ctl.drain), 0, p);
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------- softmax
@@ -526,7 +541,7 @@ attn_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
     if (warp == kLoadWarp) {
       if (lane == 0) load_role<D>(&tmQ, &tmK, &tmV, ctl, p, sQ0, sQ1, sKV);
     } else if (warp == kMmaWarp) {
-      if (lane == 0) mma_role<D>(ctl, p, tmem, sQ0, sQ1, sKV);
+      mma_role<D>(ctl, p, tmem, sQ0, sQ1, sKV);
     }
   }
 
