@@ -330,40 +330,73 @@ def run_ours(args, w, dist):
     flops = w.metric_flops()
     value = dist.world * flops / (mean_ms * 1e-3) / 1e12
 
-    # end to end: pinned host inputs -> device, forward, outputs -> pinned host
+    # End to end through the public API: every step copies its inputs from
+    # pinned host memory and its outputs (O and LSE) back to pinned host
+    # memory. Copies run on their own streams with two device buffer sets, so
+    # step i+1's upload and step i-1's download overlap step i's forward (a
+    # pipelined serving loop); the timed region spans all K steps' copies.
     hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
-    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    ho = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for _ in range(2)]
+    hl = [torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True) for _ in range(2)]
+    dq = [q, q.clone()]
+    dk = [k, k.clone()]
+    dv = [v, v.clone()]
+    do_ = [o, torch.empty_like(o)]
+    dl = [lse, torch.empty_like(lse)]
+    s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        step()
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
+    def e2e_run(nsteps):
+        ev_up = [torch.cuda.Event() for _ in range(nsteps)]
+        ev_fw = [torch.cuda.Event() for _ in range(nsteps)]
+        ev_dn = [torch.cuda.Event() for _ in range(nsteps)]
+        for i in range(nsteps):
+            b = i % 2
+            with torch.cuda.stream(s_up):
+                if i >= 2:
+                    s_up.wait_event(ev_fw[i - 2])
+                dq[b].copy_(hq, non_blocking=True)
+                dk[b].copy_(hk, non_blocking=True)
+                dv[b].copy_(hv, non_blocking=True)
+                ev_up[i].record(s_up)
+            stream.wait_event(ev_up[i])
+            if i >= 2:
+                stream.wait_event(ev_dn[i - 2])
+            st = cg.attn_prefill_fwd(dq[b], dk[b], dv[b], do_[b], dl[b], w.B, w.L, w.n_q, w.n_kv,
+                                     w.d_h, int(w.causal), w.scale, sh)
+            if st != cg.ATTN_OK:
+                raise cg.AttnError(st, "attn_prefill_fwd")
+            ev_fw[i].record(stream)
+            with torch.cuda.stream(s_down):
+                s_down.wait_event(ev_fw[i])
+                ho[b].copy_(do_[b], non_blocking=True)
+                hl[b].copy_(dl[b], non_blocking=True)
+                ev_dn[i].record(s_down)
+        stream.wait_event(ev_dn[nsteps - 1])
 
-    for _ in range(args.warmup):
-        flush.zero_()
-        e2e_step()
-    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    dist.barrier()
-    torch.cuda.synchronize()
-    for s, e in ev2:
-        flush.zero_()
-        s.record(stream)
-        e2e_step()
-        e.record(stream)
+    e2e_run(args.warmup)
     torch.cuda.synchronize()
     dist.barrier()
-    e2e_ms = dist.max(statistics.mean(s.elapsed_time(e) for s, e in ev2))
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    e2e_run(args.steps)
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    e2e_ms = dist.max(e_start.elapsed_time(e_end) / args.steps)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    d2h = ho[0].numel() * ho[0].element_size() + hl[0].numel() * hl[0].element_size()
     e2e_value = dist.world * flops / (e2e_ms * 1e-3) / 1e12
 
     peaks, peak_src = measured_peaks()
-    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    burst = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    sustained = float(peaks.get("bf16_tflops_sustained", burst))
+    # A timed window long enough to hit the power cap is a sustained run: it
+    # is compared with the dense bf16 rate measured under the same cap.
+    capped = "sw_power_cap" in clocks.get("reasons", []) and clocks.get("window") == "timed"
+    peak = sustained if capped else burst
+    peak_note = (f"bf16_tflops_sustained ({peak_src}; power cap active in the timed window)"
+                 if capped else f"bf16_tflops ({peak_src}, burst)")
     achieved = flops / (statistics.mean(step_ms) * 1e-3) / 1e12
     traffic = recorded_traffic(w.number)
     line = {
@@ -374,14 +407,17 @@ def run_ours(args, w, dist):
         "config": dict(w.describe(), parallelism=f"replicas x{dist.world}",
                        l2="flushed before every step (256 MiB device write, outside the timed interval)"),
         "pct_of_bf16_peak": 100.0 * achieved / peak,
+        "pct_of_bf16_burst": 100.0 * achieved / burst,
+        "pct_of_bf16_sustained": 100.0 * achieved / sustained,
         "gbs_io": w.io_bytes() / (statistics.mean(step_ms) * 1e-3) / 1e9,
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "note": "pinned host buffers; uploads, forward and downloads on three streams, "
+                        "two device buffer sets, no L2 flush"},
         "gpu_launches": args.steps,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                     "frac": achieved / peak, "peak_source": f"bf16_tflops ({peak_src}, burst)",
-                     "traffic": traffic},
+                     "frac": achieved / peak, "peak_source": peak_note, "traffic": traffic},
         "step_ms_min": min(step_ms), "wall_s_timed": t_wall,
         "grid": cg.attn_prefill_grid_size(w.B, w.L, w.n_q, w.n_kv, w.d_h, w.causal),
     }
