@@ -56,17 +56,20 @@ def _inputs(B, L, n_q, n_kv, d, seed=0, bf16=True):
 
 
 def brute_force(q, k, v, causal, scale):
-    """Pure-Python attention: exact sums, exp of the raw scores, LSE = log Z."""
+    """Pure-Python attention: exact sums, exp of the raw scores, LSE = log Z.
+
+    q may hold fewer rows than k, v: they are the last rows of the sequence."""
     B, L, n_q, d = q.shape
     n_kv = k.shape[2]
     g = n_q // n_kv
+    off = k.shape[1] - L
     o = np.zeros(q.shape)
     lse = np.zeros((B, n_q, L))
     for b in range(B):
         for h in range(n_q):
             kvh = h // g
             for i in range(L):
-                keys = range(i + 1) if causal else range(L)
+                keys = range(i + off + 1) if causal else range(k.shape[1])
                 sc = [scale * math.fsum(float(q[b, i, h, t]) * float(k[b, j, kvh, t])
                                         for t in range(d)) for j in keys]
                 w = [math.exp(x) for x in sc]
@@ -265,7 +268,51 @@ def pin_tiled_blocks(att):
     return worst <= 4 * gold["max_abs_difference_bound"], worst
 
 
-PINS = [pin_bruteforce, pin_sdpa, pin_row0, pin_constant_v, pin_scale_zero,
+def pin_chunk_bruteforce(att):
+    """A query chunk at the end of a longer key range, against brute force."""
+    worst = 0.0
+    for (B, Lq, Lk, n_q, n_kv, d, causal) in [(2, 3, 7, 4, 2, 4, True), (1, 5, 11, 3, 1, 3, True),
+                                               (1, 4, 9, 2, 2, 8, False)]:
+        q, _, _ = _inputs(B, Lq, n_q, n_kv, d, seed=Lq * 13 + Lk)
+        _, k, v = _inputs(B, Lk, n_q, n_kv, d, seed=Lk * 17 + Lq)
+        scale = 1.0 / math.sqrt(d)
+        o, lse = att.attention(q, k, v, causal=causal, scale=scale)
+        ob, lb = brute_force(q, k, v, causal, scale)
+        worst = max(worst, np.abs(o - ob).max(), np.abs(lse - lb).max())
+    return worst <= 1e-13, worst
+
+
+def pin_chunk_is_suffix(att):
+    """Chunked prefill reproduces the last rows of one full causal pass: the
+    chunk's rows are rows Lk-Lq.. of the square problem on the whole sequence."""
+    worst = 0.0
+    for (Lq, Lk) in [(37, 100), (64, 64), (1, 50), (50, 51)]:
+        qf, k, v = _inputs(2, Lk, 6, 2, 16, seed=Lq + 3 * Lk)
+        o_full, l_full = att.attention(qf, k, v, causal=True)
+        o, lse = att.attention(qf[:, Lk - Lq:], k, v, causal=True)
+        worst = max(worst, np.abs(o - o_full[:, Lk - Lq:]).max(),
+                    np.abs(lse - l_full[:, :, Lk - Lq:]).max())
+    return worst <= 1e-14, worst
+
+
+def pin_chunk_sdpa(att):
+    """Library check with an explicit bottom-right causal mask."""
+    torch = pytest.importorskip("torch")
+    B, Lq, Lk, n_q, n_kv, d = 2, 23, 61, 4, 2, 16
+    q, _, _ = _inputs(B, Lq, n_q, n_kv, d, seed=41)
+    _, k, v = _inputs(B, Lk, n_q, n_kv, d, seed=43)
+    o, _ = att.attention(q, k, v, causal=True)
+    keep = torch.ones(Lq, Lk, dtype=torch.bool).tril(diagonal=Lk - Lq)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q).permute(0, 2, 1, 3),
+        torch.from_numpy(np.repeat(k, 2, axis=2)).permute(0, 2, 1, 3),
+        torch.from_numpy(np.repeat(v, 2, axis=2)).permute(0, 2, 1, 3),
+        attn_mask=keep).permute(0, 2, 1, 3).numpy()
+    worst = np.abs(o - ref).max()
+    return worst <= 1e-13, worst
+
+
+PINS = [pin_bruteforce, pin_chunk_bruteforce, pin_chunk_is_suffix, pin_chunk_sdpa, pin_sdpa, pin_row0, pin_constant_v, pin_scale_zero,
         pin_gqa_equals_mha, pin_shift_invariance, pin_onehot_weights, pin_tiled_blocks]
 
 
@@ -372,13 +419,14 @@ def test_long_context_shape_costs():
 # break at least one pin
 
 MUTANTS = {
-    "mask_excludes_diagonal": ("keys[None, :] <= row_idx[:, None]", "keys[None, :] < row_idx[:, None]"),
+    "mask_excludes_diagonal": ("keys[None, :] <= pos[:, None]", "keys[None, :] < pos[:, None]"),
     "kv_head_modulo": ("kvh = h // g", "kvh = h % n_kv"),
     "scale_dropped": ("s = scale * (qrows @ krows.T)", "s = (qrows @ krows.T)"),
     "lse_without_max": ("lse = m_safe + np.log(l)", "lse = np.log(l)"),
     "no_max_subtraction": ("p = np.exp(s - m_safe[:, None])", "p = np.exp(s)"),
     "values_reversed": ("o = (p @ vrows) / l[:, None]", "o = (p @ vrows[::-1]) / l[:, None]"),
-    "prefix_off_by_one": ("lk = int(sel[-1]) + 1 if causal else L", "lk = int(sel[-1]) if causal else L"),
+    "prefix_off_by_one": ("lv = int(pos[-1]) + 1 if causal else Lk", "lv = int(pos[-1]) if causal else Lk"),
+    "chunk_aligned_top_left": ("offset = Lk - L", "offset = 0"),
     "max_over_keys_axis": ("m = s.max(axis=1)", "m = s.max(axis=0)"),
     "normalise_by_max": ("o = (p @ vrows) / l[:, None]", "o = (p @ vrows) / p.max(axis=1)[:, None]"),
 }
