@@ -199,9 +199,10 @@ def oracle_sample(w, q_host, k_host, v_host, rng, rows_per_chunk, seconds=None, 
         rows = np.stack([b, h, i], axis=1)
         qv = q_host[b, i, h]
         t0 = time.perf_counter()
-        oracle.attention_rows(qv, k_host, v_host, rows, causal=w.causal, scale=w.scale, n_q=w.n_q)
+        oracle.attention_rows(qv, k_host, v_host, rows, causal=w.causal, scale=w.scale, n_q=w.n_q,
+                              lq=w.L)
         spent += time.perf_counter() - t0
-        keys = (i + 1) if w.causal else np.full_like(i, w.L)
+        keys = (i + w.offset + 1) if w.causal else np.full_like(i, w.keys)
         flops += float((4.0 * w.d_h * keys).sum())
         nrows += rows_per_chunk
         done += 1
@@ -291,11 +292,19 @@ def run_ours(args, w, dist):
     stream = torch.cuda.current_stream(dev)
     sh = int(stream.cuda_stream)
 
-    def step():
-        st = cg.attn_prefill_fwd(q, k, v, o, lse, w.B, w.L, w.n_q, w.n_kv, w.d_h, int(w.causal),
-                                 w.scale, sh)
+    def fwd(q_, k_, v_, o_, l_):
+        # one launch of the C entry point for this workload (chunked when Lk > L)
+        if w.keys == w.L:
+            st = cg.attn_prefill_fwd(q_, k_, v_, o_, l_, w.B, w.L, w.n_q, w.n_kv, w.d_h,
+                                     int(w.causal), w.scale, sh)
+        else:
+            st = cg.attn_prefill_fwd_chunk(q_, k_, v_, o_, l_, w.B, w.L, w.keys, w.n_q, w.n_kv,
+                                           w.d_h, int(w.causal), w.scale, sh)
         if st != cg.ATTN_OK:
-            raise cg.AttnError(st, "attn_prefill_fwd")
+            raise cg.AttnError(st, "attention forward")
+
+    def step():
+        fwd(q, k, v, o, lse)
 
     sampler = ClockSampler(dist.local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
     sampler.start()
@@ -361,10 +370,7 @@ def run_ours(args, w, dist):
             stream.wait_event(ev_up[i])
             if i >= 2:
                 stream.wait_event(ev_dn[i - 2])
-            st = cg.attn_prefill_fwd(dq[b], dk[b], dv[b], do_[b], dl[b], w.B, w.L, w.n_q, w.n_kv,
-                                     w.d_h, int(w.causal), w.scale, sh)
-            if st != cg.ATTN_OK:
-                raise cg.AttnError(st, "attn_prefill_fwd")
+            fwd(dq[b], dk[b], dv[b], do_[b], dl[b])
             ev_fw[i].record(stream)
             with torch.cuda.stream(s_down):
                 s_down.wait_event(ev_fw[i])

@@ -49,6 +49,16 @@ def attn_prefill_fwd(q, k, v, o, lse, B, L, n_q, n_kv, d_h, causal, scale, strea
                                     _stream_handle(stream)))
 
 
+def attn_prefill_fwd_chunk(q, k, v, o, lse, B, Lq, Lk, n_q, n_kv, d_h, causal, scale,
+                           stream=None) -> int:
+    """Direct call of the chunked-prefill C entry point (query = last Lq of Lk
+    positions); returns the raw status code."""
+    lib = _abi.load()
+    return int(lib.attn_prefill_fwd_chunk(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B),
+                                          int(Lq), int(Lk), int(n_q), int(n_kv), int(d_h),
+                                          int(causal), float(scale), _stream_handle(stream)))
+
+
 def attn_device_check(stream=None) -> int:
     """Synchronise the stream and report device-side timeouts (raw status)."""
     return int(_abi.load().attn_device_check(_stream_handle(stream)))
@@ -61,11 +71,13 @@ def attn_prefill_grid_size(B, L, n_q, n_kv, d_h, causal=True) -> int:
 
 def attn_prefill(q, k, v, *, causal: bool = True, scale: float | None = None, out=None, lse=None,
                  stream=None):
-    """O, LSE = attention(q, k, v) for bf16 CUDA tensors q [B,L,n_q,d], k/v [B,L,n_kv,d].
+    """O, LSE = attention(q, k, v) for bf16 CUDA tensors q [B,Lq,n_q,d], k/v [B,Lk,n_kv,d].
 
-    Returns (o bf16 [B, L, n_q, d], lse fp32 [B, n_q, L]). ``scale`` defaults
-    to 1/sqrt(d). Outputs may be passed in (``out``, ``lse``) to avoid
-    allocation. The call is asynchronous on ``stream`` (default: current).
+    Lk = Lq is ordinary prefill; Lk > Lq is a chunk whose rows are the last Lq
+    positions of the key range (chunked prefill). Returns (o bf16
+    [B, Lq, n_q, d], lse fp32 [B, n_q, Lq]). ``scale`` defaults to 1/sqrt(d).
+    Outputs may be passed in (``out``, ``lse``) to avoid allocation. The call
+    is asynchronous on ``stream`` (default: current).
     """
     import torch
 
@@ -77,9 +89,9 @@ def attn_prefill(q, k, v, *, causal: bool = True, scale: float | None = None, ou
         if t.dim() != 4 or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous [B, L, H, d_h] tensor")
     B, L, n_q, d = q.shape
-    if k.shape != v.shape or k.shape[0] != B or k.shape[1] != L or k.shape[3] != d:
-        raise ValueError("k and v must be [B, L, n_kv, d_h] matching q")
-    n_kv = k.shape[2]
+    if k.shape != v.shape or k.shape[0] != B or k.shape[1] < L or k.shape[3] != d:
+        raise ValueError("k and v must be [B, Lk, n_kv, d_h] with Lk >= Lq, matching q")
+    Lk, n_kv = k.shape[1], k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
@@ -90,7 +102,12 @@ def attn_prefill(q, k, v, *, causal: bool = True, scale: float | None = None, ou
         lse = torch.empty((B, n_q, L), dtype=torch.float32, device=q.device)
     elif tuple(lse.shape) != (B, n_q, L) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous float32 [B, n_q, L] tensor")
-    st = attn_prefill_fwd(q, k, v, out, lse, B, L, n_q, n_kv, d, int(bool(causal)), scale, stream)
+    if Lk == L:
+        st = attn_prefill_fwd(q, k, v, out, lse, B, L, n_q, n_kv, d, int(bool(causal)), scale,
+                              stream)
+    else:
+        st = attn_prefill_fwd_chunk(q, k, v, out, lse, B, L, Lk, n_q, n_kv, d,
+                                    int(bool(causal)), scale, stream)
     if st != _abi.ATTN_OK:
-        raise AttnError(st, "attn_prefill_fwd")
+        raise AttnError(st, "attn_prefill_fwd" if Lk == L else "attn_prefill_fwd_chunk")
     return out, lse

@@ -84,7 +84,10 @@ struct Params {
   uint16_t* o;          // bf16 [B, L, n_q, D]
   float* lse;           // fp32 [B, n_q, L]
   int* status;          // per-device status word
-  int L, n_q, n_kv, g, T;
+  int Lq, Lk;           // query rows (chunk length) and keys
+  int offset;           // absolute position of query row 0 = Lk - Lq
+  int n_q, n_kv, g;
+  int Tq, Tk;           // 128-row query tiles and 128-key tiles
   int causal;
   int scale_pos;        // 1 when c > 0
   float c;              // scale * log2(e)
@@ -109,6 +112,8 @@ struct Unit {
 
 // Unit u -> (batch, K/V head, two query tiles). Units are ordered by pair
 // index first, so ascending u means descending causal length (longest first).
+// Query row i of the chunk sits at absolute position offset + i (the chunk is
+// the end of the key range; offset = 0 for square prefill).
 // Within one (b, kv-head) group the g*T query tiles are listed longest first
 // and paired neighbour by neighbour: slot 1 holds the longer (or equal) tile,
 // slot 0 the next one, and their key-tile counts differ by at most one.
@@ -118,15 +123,17 @@ __device__ __forceinline__ Unit decode_unit(int u, const Params& p) {
   const int grp = u - pair * p.groups;
   x.b = grp / p.n_kv;
   x.kvh = grp - x.b * p.n_kv;
-  const int total = p.g * p.T;
+  const int total = p.g * p.Tq;
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
     const int k = 2 * pair + (1 - s);
     if (k < total) {
-      const int i = p.T - 1 - k / p.g;
+      const int i = p.Tq - 1 - k / p.g;
       x.head[s] = x.kvh * p.g + (k % p.g);
       x.qtile[s] = i;
-      x.n[s] = p.causal ? i + 1 : p.T;
+      // Causal: key tiles up to the one holding the tile's last query position.
+      const int last_row = min(i * kBM + kBM - 1, p.Lq - 1);
+      x.n[s] = p.causal ? min(p.Tk, (p.offset + last_row) / kBN + 1) : p.Tk;
     } else {
       x.head[s] = 0;
       x.qtile[s] = 0;
@@ -374,7 +381,8 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem)
     const Unit x = decode_unit(u, p);
     const int n = x.n[slot];
     if (n == 0) continue;
-    const int row = x.qtile[slot] * kBM + r;
+    const int row = x.qtile[slot] * kBM + r;                    // chunk row
+    const int qrow0 = p.offset + x.qtile[slot] * kBM;           // absolute position of row 0
     float m_run = -INFINITY, l_run = 0.0f;
     for (int j = 0; j < n; ++j) {
       if (!__all_sync(0xffffffffu, wait_phase(bar_s, ph_s, ctl, p))) return;
@@ -397,18 +405,15 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem)
 #pragma unroll
         for (int i = 0; i < 128; ++i) s[i] *= p.c;
       }
-      if (j == n - 1) {
-        if (p.causal) {
-          // Diagonal tile: key kBN*j + i against query kBM*qtile + r.
+      // Keys after in-tile index `keep` are masked: past the row's absolute
+      // position (causal; the diagonal tile, or the last two tiles when the
+      // chunk offset is not a multiple of the tile), or past the last key.
+      const bool masked = p.causal ? (j * kBN + kBN - 1 > qrow0) : (p.Lk - j * kBN < kBN);
+      if (masked) {
+        const int keep = p.causal ? qrow0 + r - j * kBN : p.Lk - 1 - j * kBN;
 #pragma unroll
-          for (int i = 0; i < 128; ++i)
-            if (i > r) s[i] = -INFINITY;
-        } else if (p.L - j * kBN < kBN) {
-          const int lim = p.L - j * kBN;
-#pragma unroll
-          for (int i = 0; i < 128; ++i)
-            if (i >= lim) s[i] = -INFINITY;
-        }
+        for (int i = 0; i < 128; ++i)
+          if (i > keep) s[i] = -INFINITY;
       }
       const float m_tile = row_max128(s) * cc;
       const float m_new = fmaxf(m_run, m_tile);
@@ -463,8 +468,8 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem)
     ph_o ^= 1;
     tc_fence_after_sync();
     const float inv_l = 1.0f / l_run;
-    const bool valid = row < p.L;
-    uint16_t* orow = p.o + ((static_cast<size_t>(x.b) * p.L + row) * p.n_q + x.head[slot]) *
+    const bool valid = row < p.Lq;
+    uint16_t* orow = p.o + ((static_cast<size_t>(x.b) * p.Lq + row) * p.n_q + x.head[slot]) *
                                static_cast<size_t>(D);
 #pragma unroll
     for (int c = 0; c < D; c += 32) {
@@ -483,7 +488,7 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem)
     }
     if (valid) {
       const float m_fin = (m_run == -INFINITY) ? 0.0f : m_run;
-      p.lse[(static_cast<size_t>(x.b) * p.n_q + x.head[slot]) * p.L + row] =
+      p.lse[(static_cast<size_t>(x.b) * p.n_q + x.head[slot]) * p.Lq + row] =
           (m_fin + log2f(l_run)) * 0.69314718055994530942f;
     }
   }
@@ -644,24 +649,26 @@ bool encode_bhld(CUtensorMap* map, const void* ptr, int D, int H, int64_t L, int
 }
 
 // Sizes -> work units; returns false when they exceed 32-bit tile indexing.
-bool count_units(int64_t B, int64_t L, int32_t n_q, int32_t n_kv, int* T_out, int* units_out) {
-  const int64_t T = (L + kBM - 1) / kBM;
+bool count_units(int64_t B, int64_t Lq, int64_t Lk, int32_t n_q, int32_t n_kv, int* Tq_out,
+                 int* units_out) {
+  const int64_t Tq = (Lq + kBM - 1) / kBM;
   const int64_t g = n_q / n_kv;
-  const int64_t pairs = (g * T + 1) / 2;
+  const int64_t pairs = (g * Tq + 1) / 2;
   const int64_t units = pairs * B * n_kv;
-  if (L > (int64_t{1} << 30) || B > (int64_t{1} << 30) || g * T > INT32_MAX ||
-      units > INT32_MAX || B * n_kv > INT32_MAX)
+  if (Lq > (int64_t{1} << 30) || Lk > (int64_t{1} << 30) || B > (int64_t{1} << 30) ||
+      g * Tq > INT32_MAX || units > INT32_MAX || B * n_kv > INT32_MAX)
     return false;
-  *T_out = static_cast<int>(T);
+  *Tq_out = static_cast<int>(Tq);
   *units_out = static_cast<int>(units);
   return true;
 }
 
 attn_status_t validate(const void* q, const void* k, const void* v, const void* o,
-                       const float* lse, int64_t B, int64_t L, int32_t n_q, int32_t n_kv,
-                       int32_t d_h, int32_t causal, float scale) {
+                       const float* lse, int64_t B, int64_t Lq, int64_t Lk, int32_t n_q,
+                       int32_t n_kv, int32_t d_h, int32_t causal, float scale) {
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
-  if (B < 1 || L < 1 || n_q < 1 || n_kv < 1 || n_q % n_kv != 0) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Lq < 1 || Lk < Lq || n_q < 1 || n_kv < 1 || n_q % n_kv != 0)
+    return ATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   auto misaligned = [](const void* ptr, uintptr_t a) {
@@ -671,41 +678,37 @@ attn_status_t validate(const void* q, const void* k, const void* v, const void* 
       misaligned(lse, 4))
     return ATTN_ERR_INVALID_ARG;
   if (d_h != 64 && d_h != 128) return ATTN_ERR_UNSUPPORTED;
-  int T = 0, units = 0;
-  if (!count_units(B, L, n_q, n_kv, &T, &units)) return ATTN_ERR_UNSUPPORTED;
+  int Tq = 0, units = 0;
+  if (!count_units(B, Lq, Lk, n_q, n_kv, &Tq, &units)) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-attn_status_t attn_prefill_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                               int64_t B, int64_t L, int32_t n_q, int32_t n_kv, int32_t d_h,
-                               int32_t causal, float scale, void* stream_ptr) {
-  const attn_status_t bad = validate(q, k, v, o, lse, B, L, n_q, n_kv, d_h, causal, scale);
-  if (bad != ATTN_OK) return bad;
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  DeviceState* st = nullptr;
-  const attn_status_t ds = device_state(stream, &st);
-  if (ds != ATTN_OK) return ds;
-
-  int T = 0, units = 0;
-  count_units(B, L, n_q, n_kv, &T, &units);
+// Encodes the tensor maps, fills the parameters and launches (arguments
+// already validated). `status` is the device status word the kernel reports
+// wait timeouts into; `sms` the device's multiprocessor count.
+attn_status_t launch_forward(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int64_t B, int64_t Lq, int64_t Lk, int32_t n_q, int32_t n_kv,
+                             int32_t d_h, int32_t causal, float scale, cudaStream_t stream,
+                             int* status, int sms) {
+  int Tq = 0, units = 0;
+  count_units(B, Lq, Lk, n_q, n_kv, &Tq, &units);
   CUtensorMap mq, mk, mv;
-  if (!encode_bhld(&mq, q, d_h, n_q, L, B) || !encode_bhld(&mk, k, d_h, n_kv, L, B) ||
-      !encode_bhld(&mv, v, d_h, n_kv, L, B))
+  if (!encode_bhld(&mq, q, d_h, n_q, Lq, B) || !encode_bhld(&mk, k, d_h, n_kv, Lk, B) ||
+      !encode_bhld(&mv, v, d_h, n_kv, Lk, B))
     return ATTN_ERR_CUDA;
 
   Params p;
   p.o = static_cast<uint16_t*>(o);
   p.lse = lse;
-  p.status = st->status;
-  p.L = static_cast<int>(L);
+  p.status = status;
+  p.Lq = static_cast<int>(Lq);
+  p.Lk = static_cast<int>(Lk);
+  p.offset = static_cast<int>(Lk - Lq);
   p.n_q = n_q;
   p.n_kv = n_kv;
   p.g = n_q / n_kv;
-  p.T = T;
+  p.Tq = Tq;
+  p.Tk = static_cast<int>((Lk + kBN - 1) / kBN);
   p.causal = causal;
   p.c = scale * 1.4426950408889634f;
   p.scale_pos = p.c > 0.0f ? 1 : 0;
@@ -713,12 +716,37 @@ attn_status_t attn_prefill_fwd(const void* q, const void* k, const void* v, void
   p.units = units;
   p.spin_limit = kSpinLimitCycles;
 
-  const int grid = units < st->sms ? units : st->sms;
+  const int grid = units < sms ? units : sms;
   if (d_h == 128)
     attn_prefill_fwd_kernel<128><<<grid, kThreads, Tile<128>::kSmemBytes, stream>>>(mq, mk, mv, p);
   else
     attn_prefill_fwd_kernel<64><<<grid, kThreads, Tile<64>::kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_prefill_fwd_chunk(const void* q, const void* k, const void* v, void* o,
+                                     float* lse, int64_t B, int64_t Lq, int64_t Lk, int32_t n_q,
+                                     int32_t n_kv, int32_t d_h, int32_t causal, float scale,
+                                     void* stream_ptr) {
+  const attn_status_t bad = validate(q, k, v, o, lse, B, Lq, Lk, n_q, n_kv, d_h, causal, scale);
+  if (bad != ATTN_OK) return bad;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  DeviceState* st = nullptr;
+  const attn_status_t ds = device_state(stream, &st);
+  if (ds != ATTN_OK) return ds;
+  return launch_forward(q, k, v, o, lse, B, Lq, Lk, n_q, n_kv, d_h, causal, scale, stream,
+                        st->status, st->sms);
+}
+
+attn_status_t attn_prefill_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int64_t B, int64_t L, int32_t n_q, int32_t n_kv, int32_t d_h,
+                               int32_t causal, float scale, void* stream_ptr) {
+  return attn_prefill_fwd_chunk(q, k, v, o, lse, B, L, L, n_q, n_kv, d_h, causal, scale,
+                                stream_ptr);
 }
 
 const char* attn_status_string(attn_status_t status) {
@@ -758,7 +786,7 @@ int64_t attn_prefill_grid_size(int64_t B, int64_t L, int32_t n_q, int32_t n_kv, 
       (d_h != 64 && d_h != 128))
     return -1;
   int T = 0, units = 0;
-  if (!count_units(B, L, n_q, n_kv, &T, &units)) return -1;
+  if (!count_units(B, L, L, n_q, n_kv, &T, &units)) return -1;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -842,45 +870,17 @@ extern "C" attn_status_t attn_prefill_fwd_noalloc(const void* q, const void* k, 
                                                   void* o, float* lse, int64_t B, int64_t L,
                                                   int32_t n_q, int32_t n_kv, int32_t d_h,
                                                   int32_t causal, float scale, void* stream_ptr) {
-  const attn_status_t bad = validate(q, k, v, o, lse, B, L, n_q, n_kv, d_h, causal, scale);
+  const attn_status_t bad = validate(q, k, v, o, lse, B, L, L, n_q, n_kv, d_h, causal, scale);
   if (bad != ATTN_OK) return bad;
   if (kNoAllocScratchNeeded > kNoAllocScratchBytes) return ATTN_ERR_UNSUPPORTED;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   NoAllocState* st = nullptr;
   const attn_status_t ds = noalloc_state(&st);
   if (ds != ATTN_OK) return ds;
-
-  int T = 0, units = 0;
-  count_units(B, L, n_q, n_kv, &T, &units);
-  CUtensorMap mq, mk, mv;
-  if (!encode_bhld(&mq, q, d_h, n_q, L, B) || !encode_bhld(&mk, k, d_h, n_kv, L, B) ||
-      !encode_bhld(&mv, v, d_h, n_kv, L, B))
-    return ATTN_ERR_CUDA;
   // The status word must start at zero for every call (the kernel only ORs
   // error bits into it).
   if (cudaMemsetAsync(st->scratch, 0, kNoAllocScratchNeeded, stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
-
-  Params p;
-  p.o = static_cast<uint16_t*>(o);
-  p.lse = lse;
-  p.status = st->scratch;
-  p.L = static_cast<int>(L);
-  p.n_q = n_q;
-  p.n_kv = n_kv;
-  p.g = n_q / n_kv;
-  p.T = T;
-  p.causal = causal;
-  p.c = scale * 1.4426950408889634f;
-  p.scale_pos = p.c > 0.0f ? 1 : 0;
-  p.groups = static_cast<int>(B * n_kv);
-  p.units = units;
-  p.spin_limit = kSpinLimitCycles;
-
-  const int grid = units < st->sms ? units : st->sms;
-  if (d_h == 128)
-    attn_prefill_fwd_kernel<128><<<grid, kThreads, Tile<128>::kSmemBytes, stream>>>(mq, mk, mv, p);
-  else
-    attn_prefill_fwd_kernel<64><<<grid, kThreads, Tile<64>::kSmemBytes, stream>>>(mq, mk, mv, p);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return launch_forward(q, k, v, o, lse, B, L, L, n_q, n_kv, d_h, causal, scale, stream,
+                        st->scratch, st->sms);
 }

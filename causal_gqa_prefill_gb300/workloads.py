@@ -28,6 +28,15 @@ class Workload:
     causal: bool = True
     heavy_k_channels: int = 0       # leading K channels drawn with std 8
     full_check: bool = True         # oracle over every row (else sampled rows)
+    Lk: int = 0                     # keys (0: = L); L < Lk makes Q the last L positions
+
+    @property
+    def keys(self) -> int:
+        return self.Lk or self.L
+
+    @property
+    def offset(self) -> int:
+        return self.keys - self.L
 
     @property
     def g(self) -> int:
@@ -42,18 +51,28 @@ class Workload:
         return self.d_h ** -0.5
 
     def metric_flops(self) -> int:
-        """Causal prefill FLOPs as the metric counts them: 2*n_q*d_h*L^2*B."""
-        f = 2 * self.n_q * self.d_h * self.L * self.L * self.B
-        return f if self.causal else 2 * f
+        """Causal prefill FLOPs as the metric counts them: 2*n_q*d_h*L^2*B.
+
+        A chunk of L rows after `offset` earlier positions counts the same
+        way, 4*d_h*(offset + i) per row i summed in the L^2/2 form:
+        2*n_q*d_h*(2*L*offset + L^2)*B (equal to the square count at offset 0).
+        """
+        if not self.causal:
+            return 4 * self.n_q * self.d_h * self.L * self.keys * self.B
+        return 2 * self.n_q * self.d_h * (2 * self.L * self.offset + self.L * self.L) * self.B
 
     def io_bytes(self) -> int:
         """Bytes read and written once: Q, K, V, O in bf16 and LSE in fp32."""
-        e = self.B * self.L * self.d_h * 2
-        return e * (2 * self.n_q + 2 * self.n_kv) + self.B * self.n_q * self.L * 4
+        e = self.B * self.d_h * 2
+        return (e * (2 * self.n_q * self.L + 2 * self.n_kv * self.keys)
+                + self.B * self.n_q * self.L * 4)
 
     def describe(self) -> dict:
-        return {"workload": self.name, "B": self.B, "L": self.L, "n_q": self.n_q,
-                "n_kv": self.n_kv, "d_h": self.d_h, "causal": self.causal}
+        d = {"workload": self.name, "B": self.B, "L": self.L, "n_q": self.n_q,
+             "n_kv": self.n_kv, "d_h": self.d_h, "causal": self.causal}
+        if self.keys != self.L:
+            d["Lk"] = self.keys
+        return d
 
 
 WORKLOADS = {
@@ -67,6 +86,13 @@ WORKLOADS = {
                 1, 32768, 64, 8, 128, heavy_k_channels=4, full_check=False),
     5: Workload(5, "long-context 36-head shape, GQA-6 (B=1, L=131072, n_q=36, n_kv=6, d_h=128)",
                 1, 131072, 36, 6, 128, full_check=False),
+    # chunked prefill: the last chunk of a prompt, attending to its whole prefix
+    6: Workload(6, "chunked prefill, Llama-3-8B-shaped layer: last 2048-token chunk of an "
+                   "8192-token prompt (B=1, Lq=2048, Lk=8192, n_q=32, n_kv=8, d_h=128)",
+                1, 2048, 32, 8, 128, Lk=8192),
+    7: Workload(7, "chunked prefill, 36-head shape: last 16384-token chunk of a 131072-token "
+                   "prompt (B=1, Lq=16384, Lk=131072, n_q=36, n_kv=6, d_h=128)",
+                1, 16384, 36, 6, 128, Lk=131072, full_check=False),
 }
 
 
@@ -77,7 +103,7 @@ def make_inputs(w: Workload, device="cuda", seed: int | None = None):
     gen = torch.Generator(device=device)
     gen.manual_seed(w.seed if seed is None else seed)
     shape_q = (w.B, w.L, w.n_q, w.d_h)
-    shape_kv = (w.B, w.L, w.n_kv, w.d_h)
+    shape_kv = (w.B, w.keys, w.n_kv, w.d_h)
     q = torch.randn(shape_q, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
     k = torch.randn(shape_kv, generator=gen, device=device, dtype=torch.float32)
     if w.heavy_k_channels:
@@ -87,9 +113,9 @@ def make_inputs(w: Workload, device="cuda", seed: int | None = None):
     return q, k, v
 
 
-def custom(B, L, n_q, n_kv, d_h, causal=True, number=0, name=None) -> Workload:
-    return Workload(number, name or f"B={B} L={L} n_q={n_q} n_kv={n_kv} d_h={d_h}",
-                    B, L, n_q, n_kv, d_h, causal)
+def custom(B, L, n_q, n_kv, d_h, causal=True, number=0, name=None, Lk=0) -> Workload:
+    return Workload(number, name or f"B={B} L={L} Lk={Lk or L} n_q={n_q} n_kv={n_kv} d_h={d_h}",
+                    B, L, n_q, n_kv, d_h, causal, Lk=Lk)
 
 
 def sampled_rows(w: Workload, count: int = 4096, tile: int = 128):

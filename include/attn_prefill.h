@@ -49,7 +49,8 @@ extern "C" {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1,  /* NULL pointer, non-positive size, n_q % n_kv != 0,
-                                non-finite scale, causal not 0/1, misaligned pointer */
+                                Lk < Lq, non-finite scale, causal not 0/1,
+                                misaligned pointer */
   ATTN_ERR_UNSUPPORTED = 2,  /* d_h not 64 or 128, sizes beyond 32-bit tile indexing,
                                 device that is not sm_103 */
   ATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call or the launch failed */
@@ -81,6 +82,26 @@ attn_status_t attn_prefill_fwd(const void* q, const void* k, const void* v,
                                int64_t B, int64_t L, int32_t n_q, int32_t n_kv,
                                int32_t d_h, int32_t causal, float scale,
                                void* stream);
+
+/*
+ * Chunked prefill: the query is the last Lq positions of a sequence whose
+ * Lk >= Lq keys and values (earlier chunks' and its own) are all present, as
+ * when a long prompt is prefilled piece by piece ("prefill-attention" flop
+ * record (phantomic12), "Workarounds": chunked prefill splits a long prompt
+ * into pieces). Query row i sits at absolute position i + Lk - Lq; with
+ * causal = 1 it attends to keys j <= i + Lk - Lq (the chunk is aligned to the
+ * end of the key range), with causal = 0 to all Lk keys.
+ *
+ *   q    bf16 [B, Lq, n_q,  d_h]       k, v  bf16 [B, Lk, n_kv, d_h]
+ *   o    bf16 [B, Lq, n_q,  d_h]       lse   fp32 [B, n_q, Lq]
+ *   1 <= Lq <= Lk; every other argument, alignment rule, ownership and error
+ *   behaviour as attn_prefill_fwd, which is this call with Lq = Lk.
+ */
+attn_status_t attn_prefill_fwd_chunk(const void* q, const void* k, const void* v,
+                                     void* o, float* lse,
+                                     int64_t B, int64_t Lq, int64_t Lk, int32_t n_q,
+                                     int32_t n_kv, int32_t d_h, int32_t causal, float scale,
+                                     void* stream);
 
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* attn_status_string(attn_status_t status);

@@ -71,7 +71,7 @@ def check_rows(q, k, v, o, lse, rows, causal=True, scale=None, what=""):
     o_sel = to_np(o[r[:, 0], r[:, 2], r[:, 1]])
     lse_sel = lse[r[:, 0], r[:, 1], r[:, 2]].cpu().numpy().astype(np.float64)
     o_ref, lse_ref = oracle.attention_rows(q_sel, to_np(k), to_np(v), rows, causal=causal,
-                                           scale=scale, n_q=n_q)
+                                           scale=scale, n_q=n_q, lq=q.shape[1])
     err = errors(o_sel, lse_sel, o_ref, lse_ref)
     assert_within(err, what)
     return err

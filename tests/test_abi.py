@@ -85,6 +85,23 @@ def test_validation_rejects_before_any_cuda_call(lib, args, expect):
     assert st == expect
 
 
+@pytest.mark.parametrize("Lq,Lk,expect", [(0, 10, cg.ATTN_ERR_INVALID_ARG),
+                                           (11, 10, cg.ATTN_ERR_INVALID_ARG),
+                                           (10, 1 << 31, cg.ATTN_ERR_UNSUPPORTED)])
+def test_chunk_validation(lib, Lq, Lk, expect):
+    st = cg.attn_prefill_fwd_chunk(FAKE, FAKE, FAKE, FAKE, FAKE, 1, Lq, Lk, 4, 2, 128, 1, 0.125,
+                                   stream=0)
+    assert st == expect
+
+
+def test_chunk_workload_flops_reduce_to_square():
+    w = workloads.custom(1, 300, 4, 2, 64, Lk=300)
+    assert w.metric_flops() == oflops.causal_attention_flops(1, 300, 4, 64)
+    c = workloads.WORKLOADS[6]
+    # rows at positions offset..offset+L-1 see offset+i+1 keys: sum of 4*d*(offset+i) in L^2/2 form
+    assert c.metric_flops() == 2 * c.n_q * c.d_h * (2 * c.L * c.offset + c.L ** 2)
+
+
 def test_grid_size_argument_errors(lib):
     assert cg.attn_prefill_grid_size(0, 128, 4, 2, 128) == -1
     assert cg.attn_prefill_grid_size(1, 128, 4, 3, 128) == -1
@@ -100,7 +117,8 @@ def test_wrapper_rejects_host_tensors():
 
 def test_metric_flops_match_the_oracle_cost_model():
     for w in workloads.WORKLOADS.values():
-        assert w.metric_flops() == oflops.causal_attention_flops(w.B, w.L, w.n_q, w.d_h)
+        if w.keys == w.L:
+            assert w.metric_flops() == oflops.causal_attention_flops(w.B, w.L, w.n_q, w.d_h)
 
 
 def test_sampled_rows_cover_heads_and_tile_positions():

@@ -153,3 +153,74 @@ def test_explicit_stream_and_preallocated_outputs():
         attn_prefill(q, k, v, out=o, lse=lse, stream=s)
     s.synchronize()
     check_full(q, k, v, o, lse, what="side stream")
+
+
+# ----------------------------------------------------------------------------
+# chunked prefill: the query is the last Lq of Lk positions
+
+CHUNKS = [
+    # B, Lq, Lk, n_q, n_kv, d_h, causal
+    (2, 300, 1000, 8, 2, 128, True),     # offset 700: diagonal spans two key tiles
+    (1, 128, 256, 4, 4, 64, True),       # aligned offset
+    (1, 1, 777, 2, 1, 128, True),        # a single new token
+    (2, 129, 1000, 6, 2, 128, True),     # g = 3, ragged chunk
+    (1, 250, 250, 4, 2, 128, True),      # Lq = Lk through the chunk entry point
+    (1, 300, 500, 4, 2, 128, False),     # full attention over the prefix
+    (1, 640, 1664, 2, 1, 64, True),      # g = 1, aligned offset 1024
+]
+
+
+@pytest.mark.parametrize("case", CHUNKS, ids=lambda c: "B%d_Lq%d_Lk%d_q%d_kv%d_d%d_%s" % (
+    c[0], c[1], c[2], c[3], c[4], c[5], "causal" if c[6] else "full"))
+def test_chunk_full(case):
+    B, Lq, Lk, n_q, n_kv, d, causal = case
+    w = W.custom(B, Lq, n_q, n_kv, d, causal, Lk=Lk)
+    q, k, v = W.make_inputs(w, "cuda", seed=hash(case) % 100000)
+    o, lse = run_gpu(q, k, v, causal=causal)
+    check_full(q, k, v, o, lse, causal=causal, what=str(case))
+
+
+@pytest.mark.parametrize("Lq,Lk", [(256, 1024), (640, 2048), (100, 1100)])
+def test_chunk_matches_suffix_of_full_pass(Lq, Lk):
+    """A chunk's rows are the last rows of one full causal pass over the whole
+    sequence; with a tile-aligned offset every query tile sees the same key
+    tiles in the same order, so the outputs are bit-identical."""
+    w = W.custom(1, Lk, 8, 2, 128)
+    qf, k, v = W.make_inputs(w, "cuda", seed=Lq + Lk)
+    o_full, l_full = run_gpu(qf, k, v)
+    q = qf[:, Lk - Lq:].contiguous()
+    o, lse = run_gpu(q, k, v)
+    if (Lk - Lq) % 128 == 0:
+        assert torch.equal(o, o_full[:, Lk - Lq:]) and torch.equal(lse, l_full[:, :, Lk - Lq:])
+    else:
+        d = (o.float() - o_full[:, Lk - Lq:].float()).abs().max().item()
+        assert d <= 1e-2
+        assert (lse - l_full[:, :, Lk - Lq:]).abs().max().item() <= 1e-3
+
+
+def test_chunked_prefill_in_pieces_equals_one_pass():
+    """Prefilling a prompt as four chunks, each attending to everything before
+    it, reproduces the single causal pass."""
+    w = W.custom(2, 1536, 4, 2, 128)
+    qf, k, v = W.make_inputs(w, "cuda", seed=91)
+    o_full, l_full = run_gpu(qf, k, v)
+    for c0, c1 in [(0, 384), (384, 768), (768, 1152), (1152, 1536)]:
+        o, lse = run_gpu(qf[:, c0:c1].contiguous(), k[:, :c1].contiguous(), v[:, :c1].contiguous())
+        assert torch.equal(o, o_full[:, c0:c1]) and torch.equal(lse, l_full[:, :, c0:c1])
+
+
+def test_chunk_workload_full():
+    w = W.WORKLOADS[6]
+    q, k, v = W.make_inputs(w, "cuda")
+    o, lse = run_gpu(q, k, v, causal=w.causal, scale=w.scale)
+    err = check_full(q, k, v, o, lse, causal=w.causal, scale=w.scale, what=w.name)
+    print(f"parity {w.name}: {err}")
+
+
+def test_chunk_workload_sampled_rows():
+    w = W.WORKLOADS[7]
+    q, k, v = W.make_inputs(w, "cuda")
+    o, lse = run_gpu(q, k, v, causal=w.causal, scale=w.scale)
+    rows = W.sampled_rows(w)
+    err = check_rows(q, k, v, o, lse, rows, causal=w.causal, scale=w.scale, what=w.name)
+    print(f"parity {w.name} ({len(rows)} sampled rows): {err}")
