@@ -59,6 +59,48 @@ def attn_prefill_fwd_chunk(q, k, v, o, lse, B, Lq, Lk, n_q, n_kv, d_h, causal, s
                                           int(causal), float(scale), _stream_handle(stream)))
 
 
+def attn_prefill_fwd_fp8(q, k, v, o, lse, B, Lq, Lk, n_q, n_kv, d_h, causal, scale, q_descale,
+                         k_descale, v_descale, stream=None) -> int:
+    """Direct call of the e4m3 C entry point; returns the raw status code."""
+    lib = _abi.load()
+    return int(lib.attn_prefill_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B),
+                                        int(Lq), int(Lk), int(n_q), int(n_kv), int(d_h),
+                                        int(causal), float(scale), float(q_descale),
+                                        float(k_descale), float(v_descale),
+                                        _stream_handle(stream)))
+
+
+def attn_prefill_fp8(q, k, v, *, q_descale=1.0, k_descale=1.0, v_descale=1.0, causal=True,
+                     scale=None, out=None, lse=None, stream=None):
+    """Attention over e4m3 CUDA tensors (torch.float8_e4m3fn) q [B,Lq,n_q,128],
+    k/v [B,Lk,n_kv,128], real values = stored * descale. Returns (o bf16
+    [B, Lq, n_q, 128], lse fp32 [B, n_q, Lq])."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if t.dtype != torch.float8_e4m3fn:
+            raise TypeError(f"{name} must be float8_e4m3fn")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B, L, H, d_h] tensor")
+    B, L, n_q, d = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[1] < L or k.shape[3] != d:
+        raise ValueError("k and v must be [B, Lk, n_kv, d_h] with Lk >= Lq, matching q")
+    Lk, n_kv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, L, n_q, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, n_q, L), dtype=torch.float32, device=q.device)
+    st = attn_prefill_fwd_fp8(q, k, v, out, lse, B, L, Lk, n_q, n_kv, d, int(bool(causal)),
+                              scale, q_descale, k_descale, v_descale, stream)
+    if st != _abi.ATTN_OK:
+        raise AttnError(st, "attn_prefill_fwd_fp8")
+    return out, lse
+
+
 def attn_device_check(stream=None) -> int:
     """Synchronise the stream and report device-side timeouts (raw status)."""
     return int(_abi.load().attn_device_check(_stream_handle(stream)))

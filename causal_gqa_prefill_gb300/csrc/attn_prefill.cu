@@ -71,13 +71,20 @@ constexpr float kRescaleThreshold = 8.0f;
 constexpr int kStatusTimeout = 1;
 constexpr long long kSpinLimitCycles = 1ll << 31;   // about a second at 2 GHz
 
-template <int D>
+// D = head dim; F8: Q, K, V (and P) in fp8 e4m3 instead of bf16.
+template <int D, bool F8>
 struct Tile {
-  static constexpr int kChunks = D / 64;               // 128-byte swizzle column chunks
-  static constexpr int kQBytes = kBM * D * 2;
-  static constexpr int kKVBytes = kBN * D * 2;
-  static constexpr int kStages = (D == 128) ? 4 : 8;   // K/V ring depth (K and V share it)
+  static constexpr int kElemBytes = F8 ? 1 : 2;
+  static constexpr int kRowBytes = D * kElemBytes;
+  static constexpr int kChunks = kRowBytes / 128;       // 128-byte swizzle column chunks
+  static constexpr int kChunkElems = 128 / kElemBytes;  // elements per chunk row
+  static constexpr int kQBytes = kBM * kRowBytes;
+  static constexpr int kKVBytes = kBN * kRowBytes;
+  static constexpr int kStages = (kKVBytes == 32768) ? 4 : 8;   // K/V ring depth (K and V share it)
   static constexpr int kSmemBytes = 2 * kQBytes + kStages * kKVBytes + 1024;
+  // MMA K step: 16 bf16 or 32 e4m3 elements, 32 bytes either way.
+  static constexpr int kKStep = 32 / kElemBytes;
+  static_assert(kRowBytes % 128 == 0, "rows must fill whole 128-byte swizzle chunks");
 };
 
 struct Params {
@@ -90,7 +97,8 @@ struct Params {
   int Tq, Tk;           // 128-row query tiles and 128-key tiles
   int causal;
   int scale_pos;        // 1 when c > 0
-  float c;              // scale * log2(e)
+  float c;              // scale * log2(e) (times the Q and K descale factors for fp8)
+  float o_scale;        // multiplies O / l in the epilogue (the V descale for fp8, else 1)
   int groups;           // B * n_kv
   int units;            // pairs per group * groups
   long long spin_limit;
@@ -186,11 +194,11 @@ __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, Ctl& ctl
 
 // ------------------------------------------------------------------ producer
 
-template <int D>
+template <int D, bool F8>
 __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                           const CUtensorMap* tmV, Ctl& ctl, const Params& p,
                           uint32_t sQ0, uint32_t sQ1, uint32_t sKV) {
-  using TL = Tile<D>;
+  using TL = Tile<D, F8>;
   // Run by lane 0 alone: a whole warp polling the ring barriers would cost
   // the softmax warps on this SM sub-partition more issue slots than it saves.
   uint32_t it = 0;       // K/V ring items issued
@@ -212,7 +220,8 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
       const uint32_t dst = s ? sQ1 : sQ0;
 #pragma unroll
       for (int c = 0; c < TL::kChunks; ++c)
-        tma_load_4d(dst + c * kBM * 128, tmQ, qbar, c * 64, x.head[s], x.qtile[s] * kBM, x.b);
+        tma_load_4d(dst + c * kBM * 128, tmQ, qbar, c * TL::kChunkElems, x.head[s], x.qtile[s] * kBM,
+                    x.b);
     }
     for (int j = 0; j < x.nkv && ok; ++j) {
 #pragma unroll
@@ -227,7 +236,8 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
         mbar_arrive_expect_tx(bar, TL::kKVBytes);
 #pragma unroll
         for (int c = 0; c < TL::kChunks; ++c)
-          tma_load_4d(dst + c * kBN * 128, kind ? tmV : tmK, bar, c * 64, x.kvh, j * kBN, x.b);
+          tma_load_4d(dst + c * kBN * 128, kind ? tmV : tmK, bar, c * TL::kChunkElems, x.kvh, j * kBN,
+                      x.b);
         ++it;
       }
     }
@@ -245,37 +255,47 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
 
 // ---------------------------------------------------------------- MMA issuer
 
-template <int D>
+template <int D, bool F8>
 __device__ __forceinline__ void issue_qk(bool leader, uint32_t d_tmem, uint32_t q_smem,
                                          uint32_t k_smem) {
-  constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false);
+  using TL = Tile<D, F8>;
+  constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(kBM, kBN, false) : idesc_bf16_f32(kBM, kBN, false);
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    // K step kk: 16 bf16 = 32 bytes inside chunk kk/4 of the swizzled tile.
+  for (int kk = 0; kk < TL::kRowBytes / 32; ++kk) {
+    // K step kk: 32 bytes (16 bf16 or 32 e4m3) inside chunk kk/4 of the swizzled tile.
     const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
     const uint64_t a = sdesc_sw128(q_smem + off, 16, 1024);
     const uint64_t b = sdesc_sw128(k_smem + off, 16, 1024);
-    if (leader) mma_ss(d_tmem, a, b, idesc, kk > 0 ? 1u : 0u);
+    if (leader) {
+      if (F8) mma_ss_e4m3(d_tmem, a, b, idesc, kk > 0 ? 1u : 0u);
+      else mma_ss(d_tmem, a, b, idesc, kk > 0 ? 1u : 0u);
+    }
   }
 }
 
-template <int D>
+template <int D, bool F8>
 __device__ __forceinline__ void issue_pv(bool leader, uint32_t d_tmem, uint32_t p_tmem,
                                          uint32_t v_smem, bool accumulate) {
-  constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, true);
+  using TL = Tile<D, F8>;
+  constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(kBM, D, true) : idesc_bf16_f32(kBM, D, true);
 #pragma unroll
-  for (int kk = 0; kk < kBN / 16; ++kk) {
-    // V tile is [keys][D] with D contiguous (MN-major for this product): 16
-    // keys = 2048 bytes per K step; 64-column chunks are kBN*128 bytes apart.
-    const uint64_t b = sdesc_sw128(v_smem + kk * 16 * 128, kBN * 128, 1024);
-    if (leader) mma_ts(d_tmem, p_tmem + kk * 8, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < kBN / TL::kKStep; ++kk) {
+    // V tile is [keys][D] with D contiguous (MN-major for this product): a K
+    // step of 16 (bf16) or 32 (e4m3) keys spans that many 128-byte rows;
+    // 128-byte column chunks are kBN*128 bytes apart. P takes 8 TMEM columns
+    // per K step either way (2 bf16 or 4 e4m3 per column).
+    const uint64_t b = sdesc_sw128(v_smem + kk * TL::kKStep * 128, kBN * 128, 1024);
+    if (leader) {
+      if (F8) mma_ts_e4m3(d_tmem, p_tmem + kk * 8, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
+      else mma_ts(d_tmem, p_tmem + kk * 8, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
+    }
   }
 }
 
-template <int D>
+template <int D, bool F8>
 __device__ void mma_role(Ctl& ctl, const Params& p, uint32_t tmem, uint32_t sQ0, uint32_t sQ1,
                          uint32_t sKV) {
-  using TL = Tile<D>;
+  using TL = Tile<D, F8>;
   // The whole warp runs this loop (so its control flow and descriptor math
   // stay warp-uniform); one elected lane issues every tcgen05 instruction,
   // which keeps all commits on the thread that issued the MMAs.
@@ -299,17 +319,17 @@ __device__ void mma_role(Ctl& ctl, const Params& p, uint32_t tmem, uint32_t sQ0,
       tc_fence_after_sync();
       const uint32_t k_smem = sKV + ks * TL::kKVBytes;
       if (j < x.n[0]) {
-        issue_qk<D>(leader, tmem + kColS0, sQ0, k_smem);
+        issue_qk<D, F8>(leader, tmem + kColS0, sQ0, k_smem);
         if (leader) mma_commit(smem_addr(&ctl.s_full[0]));
       }
       if (j > 0) {
         if (!wait_all(smem_addr(&ctl.p_full[1]), ph_p1, ctl, p)) { ok = false; break; }
         ph_p1 ^= 1;
         tc_fence_after_sync();
-        issue_pv<D>(leader, tmem + kColO1, tmem + kColS1, sKV + v_prev * TL::kKVBytes, j - 1 > 0);
+        issue_pv<D, F8>(leader, tmem + kColO1, tmem + kColS1, sKV + v_prev * TL::kKVBytes, j - 1 > 0);
         if (leader) mma_commit(smem_addr(&ctl.kv_empty[v_prev]));
       }
-      issue_qk<D>(leader, tmem + kColS1, sQ1, k_smem);
+      issue_qk<D, F8>(leader, tmem + kColS1, sQ1, k_smem);
       if (leader) mma_commit(smem_addr(&ctl.s_full[1]));
       if (leader) mma_commit(smem_addr(&ctl.kv_empty[ks]));
       if (leader && j == x.nkv - 1) mma_commit(smem_addr(&ctl.q_empty));
@@ -322,7 +342,7 @@ __device__ void mma_role(Ctl& ctl, const Params& p, uint32_t tmem, uint32_t sQ0,
         if (!wait_all(smem_addr(&ctl.p_full[0]), ph_p0, ctl, p)) { ok = false; break; }
         ph_p0 ^= 1;
         tc_fence_after_sync();
-        issue_pv<D>(leader, tmem + kColO0, tmem + kColS0, sKV + vs * TL::kKVBytes, j > 0);
+        issue_pv<D, F8>(leader, tmem + kColO0, tmem + kColS0, sKV + vs * TL::kKVBytes, j > 0);
         if (leader && j == x.n[0] - 1) mma_commit(smem_addr(&ctl.o_done[0]));
       }
       v_prev = vs;
@@ -331,7 +351,7 @@ __device__ void mma_role(Ctl& ctl, const Params& p, uint32_t tmem, uint32_t sQ0,
     if (!wait_all(smem_addr(&ctl.p_full[1]), ph_p1, ctl, p)) break;
     ph_p1 ^= 1;
     tc_fence_after_sync();
-    issue_pv<D>(leader, tmem + kColO1, tmem + kColS1, sKV + v_prev * TL::kKVBytes, x.nkv - 1 > 0);
+    issue_pv<D, F8>(leader, tmem + kColO1, tmem + kColS1, sKV + v_prev * TL::kKVBytes, x.nkv - 1 > 0);
     if (leader) mma_commit(smem_addr(&ctl.o_done[1]));
     if (leader) mma_commit(smem_addr(&ctl.kv_empty[v_prev]));
   }
@@ -361,7 +381,7 @@ __device__ __forceinline__ float row_max128(const float* v) {
   return max3(max3(m[0], m[1], m[2]), max3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
 }
 
-template <int D>
+template <int D, bool F8>
 __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = (warp & 3) * 32 + lane;                         // tile row = TMEM lane
@@ -434,27 +454,49 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem)
           tmem_st32(tO + c, ov);
         }
       }
-      // P = 2^(c*s - m) as bf16 pairs into columns [0, 64) of this tile's S
-      // region (every score of the row is already in registers). Two scores
-      // per packed FMA / add.
+      // P = 2^(c*s - m) into the first columns of this tile's S region (every
+      // score of the row is already in registers): bf16 pairs in [0, 64), or
+      // e4m3 quadruples in [0, 32). Two scores per packed FMA / add.
       const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
       const uint64_t negm2 = f32x2_pack(-m_use, -m_use);
       uint64_t sum2 = f32x2_pack(0.0f, 0.0f);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      if (F8) {
+        // e4m3 P, four scores per TMEM column (first key in the lowest byte),
+        // columns [0, 32). The row sum keeps the unrounded fp32 values.
+        uint64_t sum2b = sum2;
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const uint64_t xa = ffma2(f32x2_pack(s[64 * h + 2 * i], s[64 * h + 2 * i + 1]), cc2, negm2);
-          float x0, x1;
+          const uint64_t xa = ffma2(f32x2_pack(s[4 * i], s[4 * i + 1]), cc2, negm2);
+          const uint64_t xb = ffma2(f32x2_pack(s[4 * i + 2], s[4 * i + 3]), cc2, negm2);
+          float x0, x1, x2, x3;
           f32x2_unpack(xa, x0, x1);
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
-          const uint64_t pp = f32x2_pack(p0, p1);
-          sum2 = fadd2(sum2, pp);
-          pk[i] = pack_bf16x2(p0, p1);
+          f32x2_unpack(xb, x2, x3);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+          sum2 = fadd2(sum2, f32x2_pack(p0, p1));
+          sum2b = fadd2(sum2b, f32x2_pack(p2, p3));
+          pk[i] = pack_e4m3x4(p0, p1, p2, p3);
         }
-        tmem_st32(tS + 32 * h, pk);
+        tmem_st32(tS, pk);
+        sum2 = fadd2(sum2, sum2b);
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const uint64_t xa = ffma2(f32x2_pack(s[64 * h + 2 * i], s[64 * h + 2 * i + 1]), cc2, negm2);
+            float x0, x1;
+            f32x2_unpack(xa, x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            const uint64_t pp = f32x2_pack(p0, p1);
+            sum2 = fadd2(sum2, pp);
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(tS + 32 * h, pk);
+        }
       }
       float sa, sb;
       f32x2_unpack(sum2, sa, sb);
@@ -467,7 +509,7 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem)
     if (!__all_sync(0xffffffffu, wait_phase(bar_o, ph_o, ctl, p))) return;
     ph_o ^= 1;
     tc_fence_after_sync();
-    const float inv_l = 1.0f / l_run;
+    const float inv_l = p.o_scale / l_run;
     const bool valid = row < p.Lq;
     uint16_t* orow = p.o + ((static_cast<size_t>(x.b) * p.Lq + row) * p.n_q + x.head[slot]) *
                                static_cast<size_t>(D);
@@ -496,12 +538,12 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem)
 
 // -------------------------------------------------------------------- kernel
 
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const Params p) {
-  using TL = Tile<D>;
+  using TL = Tile<D, F8>;
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Ctl ctl;
   const uint32_t base = (smem_addr(dyn_smem) + 1023u) & ~1023u;   // swizzle atoms need 1 KiB
@@ -540,13 +582,13 @@ attn_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
 
   if (warp < 8) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
-    softmax_role<D>(warp >> 2, ctl, p, tmem);
+    softmax_role<D, F8>(warp >> 2, ctl, p, tmem);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
     if (warp == kLoadWarp) {
-      if (lane == 0) load_role<D>(&tmQ, &tmK, &tmV, ctl, p, sQ0, sQ1, sKV);
+      if (lane == 0) load_role<D, F8>(&tmQ, &tmK, &tmV, ctl, p, sQ0, sQ1, sKV);
     } else if (warp == kMmaWarp) {
-      mma_role<D>(ctl, p, tmem, sQ0, sQ1, sKV);
+      mma_role<D, F8>(ctl, p, tmem, sQ0, sQ1, sKV);
     }
   }
 
@@ -579,15 +621,21 @@ EncodeTiledFn g_encode = nullptr;
 // The softmax warpgroups raise their register limit with setmaxnreg; that
 // only succeeds if the CTA was launched with at least kRegBudget registers,
 // so refuse to launch a build whose register count does not cover the split.
-bool kernel_registers_fit() {
+template <int D, bool F8>
+bool configure_kernel() {
   cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, attn_prefill_fwd_kernel<128>) != cudaSuccess ||
+  if (cudaFuncGetAttributes(&fa, attn_prefill_fwd_kernel<D, F8>) != cudaSuccess ||
       fa.numRegs * kThreads < kRegBudget)
     return false;
-  if (cudaFuncGetAttributes(&fa, attn_prefill_fwd_kernel<64>) != cudaSuccess ||
-      fa.numRegs * kThreads < kRegBudget)
-    return false;
-  return true;
+  return cudaFuncSetAttribute(attn_prefill_fwd_kernel<D, F8>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Tile<D, F8>::kSmemBytes) == cudaSuccess;
+}
+
+// Register-split check and shared-memory limit for every kernel instance.
+bool configure_kernels() {
+  return configure_kernel<64, false>() && configure_kernel<128, false>() &&
+         configure_kernel<128, true>();
 }
 
 attn_status_t device_state(cudaStream_t stream, DeviceState** out) {
@@ -603,7 +651,7 @@ attn_status_t device_state(cudaStream_t stream, DeviceState** out) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return ATTN_ERR_CUDA;
     if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;   // built for sm_103a only
-    if (!kernel_registers_fit()) return ATTN_ERR_UNSUPPORTED;
+    if (!configure_kernels()) return ATTN_ERR_UNSUPPORTED;
     if (!g_encode) {
       cudaDriverEntryPointQueryResult q;
       void* fn = nullptr;
@@ -613,11 +661,6 @@ attn_status_t device_state(cudaStream_t stream, DeviceState** out) {
         return ATTN_ERR_CUDA;
       g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
-    if (cudaFuncSetAttribute(attn_prefill_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Tile<64>::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(attn_prefill_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Tile<128>::kSmemBytes) != cudaSuccess)
-      return ATTN_ERR_CUDA;
     int* status = nullptr;
     if (cudaMalloc(&status, 256) != cudaSuccess) return ATTN_ERR_CUDA;
     if (cudaMemsetAsync(status, 0, 256, stream) != cudaSuccess) {
@@ -632,17 +675,21 @@ attn_status_t device_state(cudaStream_t stream, DeviceState** out) {
   return ATTN_OK;
 }
 
-// [B, L, H, D] bf16 as a 4-D tensor (D, H, L, B); boxes of 64 x 1 x 128 x 1
-// with 128-byte swizzle. Rows past L read as zeros.
-bool encode_bhld(CUtensorMap* map, const void* ptr, int D, int H, int64_t L, int64_t B) {
+// [B, L, H, D] (bf16, or e4m3 bytes when f8) as a 4-D tensor (D, H, L, B);
+// boxes of one 128-byte row chunk x 1 x 128 x 1 with 128-byte swizzle. Rows
+// past L read as zeros.
+bool encode_bhld(CUtensorMap* map, const void* ptr, int D, int H, int64_t L, int64_t B,
+                 bool f8 = false) {
+  const cuuint64_t eb = f8 ? 1 : 2;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
                               static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(B)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
-                                 static_cast<cuuint64_t>(H) * D * 2,
-                                 static_cast<cuuint64_t>(L) * H * D * 2};
-  const cuuint32_t box[4] = {64, 1, kBM, 1};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * eb,
+                                 static_cast<cuuint64_t>(H) * D * eb,
+                                 static_cast<cuuint64_t>(L) * H * D * eb};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / eb), 1, kBM, 1};
   const cuuint32_t estride[4] = {1, 1, 1, 1};
-  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides,
+  return g_encode(map, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                  const_cast<void*>(ptr), dims, strides,
                   box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -686,15 +733,18 @@ attn_status_t validate(const void* q, const void* k, const void* v, const void* 
 // Encodes the tensor maps, fills the parameters and launches (arguments
 // already validated). `status` is the device status word the kernel reports
 // wait timeouts into; `sms` the device's multiprocessor count.
+// f8: Q, K, V are e4m3 with the given descale factors (real value = stored
+// value * descale); otherwise bf16 and the descales are 1.
 attn_status_t launch_forward(const void* q, const void* k, const void* v, void* o, float* lse,
                              int64_t B, int64_t Lq, int64_t Lk, int32_t n_q, int32_t n_kv,
                              int32_t d_h, int32_t causal, float scale, cudaStream_t stream,
-                             int* status, int sms) {
+                             int* status, int sms, bool f8 = false, float qk_descale = 1.0f,
+                             float v_descale = 1.0f) {
   int Tq = 0, units = 0;
   count_units(B, Lq, Lk, n_q, n_kv, &Tq, &units);
   CUtensorMap mq, mk, mv;
-  if (!encode_bhld(&mq, q, d_h, n_q, Lq, B) || !encode_bhld(&mk, k, d_h, n_kv, Lk, B) ||
-      !encode_bhld(&mv, v, d_h, n_kv, Lk, B))
+  if (!encode_bhld(&mq, q, d_h, n_q, Lq, B, f8) || !encode_bhld(&mk, k, d_h, n_kv, Lk, B, f8) ||
+      !encode_bhld(&mv, v, d_h, n_kv, Lk, B, f8))
     return ATTN_ERR_CUDA;
 
   Params p;
@@ -710,17 +760,23 @@ attn_status_t launch_forward(const void* q, const void* k, const void* v, void* 
   p.Tq = Tq;
   p.Tk = static_cast<int>((Lk + kBN - 1) / kBN);
   p.causal = causal;
-  p.c = scale * 1.4426950408889634f;
+  p.c = scale * qk_descale * 1.4426950408889634f;
+  p.o_scale = v_descale;
   p.scale_pos = p.c > 0.0f ? 1 : 0;
   p.groups = static_cast<int>(B * n_kv);
   p.units = units;
   p.spin_limit = kSpinLimitCycles;
 
   const int grid = units < sms ? units : sms;
-  if (d_h == 128)
-    attn_prefill_fwd_kernel<128><<<grid, kThreads, Tile<128>::kSmemBytes, stream>>>(mq, mk, mv, p);
+  if (f8)
+    attn_prefill_fwd_kernel<128, true>
+        <<<grid, kThreads, Tile<128, true>::kSmemBytes, stream>>>(mq, mk, mv, p);
+  else if (d_h == 128)
+    attn_prefill_fwd_kernel<128, false>
+        <<<grid, kThreads, Tile<128, false>::kSmemBytes, stream>>>(mq, mk, mv, p);
   else
-    attn_prefill_fwd_kernel<64><<<grid, kThreads, Tile<64>::kSmemBytes, stream>>>(mq, mk, mv, p);
+    attn_prefill_fwd_kernel<64, false>
+        <<<grid, kThreads, Tile<64, false>::kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -747,6 +803,25 @@ attn_status_t attn_prefill_fwd(const void* q, const void* k, const void* v, void
                                int32_t causal, float scale, void* stream_ptr) {
   return attn_prefill_fwd_chunk(q, k, v, o, lse, B, L, L, n_q, n_kv, d_h, causal, scale,
                                 stream_ptr);
+}
+
+attn_status_t attn_prefill_fwd_fp8(const void* q, const void* k, const void* v, void* o,
+                                   float* lse, int64_t B, int64_t Lq, int64_t Lk, int32_t n_q,
+                                   int32_t n_kv, int32_t d_h, int32_t causal, float scale,
+                                   float q_descale, float k_descale, float v_descale,
+                                   void* stream_ptr) {
+  const attn_status_t bad = validate(q, k, v, o, lse, B, Lq, Lk, n_q, n_kv, d_h, causal, scale);
+  if (bad != ATTN_OK) return bad;
+  if (!std::isfinite(q_descale) || !std::isfinite(k_descale) || !std::isfinite(v_descale) ||
+      !std::isfinite(scale * q_descale * k_descale))
+    return ATTN_ERR_INVALID_ARG;
+  if (d_h != 128) return ATTN_ERR_UNSUPPORTED;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  DeviceState* st = nullptr;
+  const attn_status_t ds = device_state(stream, &st);
+  if (ds != ATTN_OK) return ds;
+  return launch_forward(q, k, v, o, lse, B, Lq, Lk, n_q, n_kv, d_h, causal, scale, stream,
+                        st->status, st->sms, true, q_descale * k_descale, v_descale);
 }
 
 const char* attn_status_string(attn_status_t status) {
@@ -838,7 +913,7 @@ attn_status_t noalloc_state(NoAllocState** out) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return ATTN_ERR_CUDA;
     if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;
-    if (!kernel_registers_fit()) return ATTN_ERR_UNSUPPORTED;
+    if (!configure_kernels()) return ATTN_ERR_UNSUPPORTED;
     if (!g_encode) {
       cudaDriverEntryPointQueryResult q;
       void* fn = nullptr;
@@ -848,11 +923,6 @@ attn_status_t noalloc_state(NoAllocState** out) {
         return ATTN_ERR_CUDA;
       g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
-    if (cudaFuncSetAttribute(attn_prefill_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Tile<64>::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(attn_prefill_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Tile<128>::kSmemBytes) != cudaSuccess)
-      return ATTN_ERR_CUDA;
     void* scratch = nullptr;
     if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || scratch == nullptr)
       return ATTN_ERR_CUDA;

@@ -29,6 +29,7 @@ class Workload:
     heavy_k_channels: int = 0       # leading K channels drawn with std 8
     full_check: bool = True         # oracle over every row (else sampled rows)
     Lk: int = 0                     # keys (0: = L); L < Lk makes Q the last L positions
+    dtype: str = "bf16"             # "bf16" or "e4m3" (Q, K, V stored as fp8, descale 1)
 
     @property
     def keys(self) -> int:
@@ -72,6 +73,8 @@ class Workload:
              "n_kv": self.n_kv, "d_h": self.d_h, "causal": self.causal}
         if self.keys != self.L:
             d["Lk"] = self.keys
+        if self.dtype != "bf16":
+            d["inputs"] = self.dtype
         return d
 
 
@@ -93,6 +96,11 @@ WORKLOADS = {
     7: Workload(7, "chunked prefill, 36-head shape: last 16384-token chunk of a 131072-token "
                    "prompt (B=1, Lq=16384, Lk=131072, n_q=36, n_kv=6, d_h=128)",
                 1, 16384, 36, 6, 128, Lk=131072, full_check=False),
+    # fp8 (e4m3) inputs on the model-shaped layers
+    8: Workload(8, "fp8 e4m3, Llama-3-8B-shaped layer, GQA-4 (B=1, L=8192, n_q=32, n_kv=8, "
+                   "d_h=128)", 1, 8192, 32, 8, 128, dtype="e4m3", full_check=False),
+    9: Workload(9, "fp8 e4m3, long-context 36-head shape, GQA-6 (B=1, L=131072, n_q=36, n_kv=6, "
+                   "d_h=128)", 1, 131072, 36, 6, 128, dtype="e4m3", full_check=False),
 }
 
 
@@ -104,18 +112,20 @@ def make_inputs(w: Workload, device="cuda", seed: int | None = None):
     gen.manual_seed(w.seed if seed is None else seed)
     shape_q = (w.B, w.L, w.n_q, w.d_h)
     shape_kv = (w.B, w.keys, w.n_kv, w.d_h)
-    q = torch.randn(shape_q, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+    dt = torch.float8_e4m3fn if w.dtype == "e4m3" else torch.bfloat16
+    q = torch.randn(shape_q, generator=gen, device=device, dtype=torch.float32).to(dt)
     k = torch.randn(shape_kv, generator=gen, device=device, dtype=torch.float32)
     if w.heavy_k_channels:
         k[..., :w.heavy_k_channels] *= 8.0
-    k = k.to(torch.bfloat16)
-    v = torch.randn(shape_kv, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+    k = k.to(dt)
+    v = torch.randn(shape_kv, generator=gen, device=device, dtype=torch.float32).to(dt)
     return q, k, v
 
 
-def custom(B, L, n_q, n_kv, d_h, causal=True, number=0, name=None, Lk=0) -> Workload:
+def custom(B, L, n_q, n_kv, d_h, causal=True, number=0, name=None, Lk=0,
+           dtype="bf16") -> Workload:
     return Workload(number, name or f"B={B} L={L} Lk={Lk or L} n_q={n_q} n_kv={n_kv} d_h={d_h}",
-                    B, L, n_q, n_kv, d_h, causal, Lk=Lk)
+                    B, L, n_q, n_kv, d_h, causal, Lk=Lk, dtype=dtype)
 
 
 def sampled_rows(w: Workload, count: int = 4096, tile: int = 128):

@@ -51,8 +51,8 @@ typedef enum {
   ATTN_ERR_INVALID_ARG = 1,  /* NULL pointer, non-positive size, n_q % n_kv != 0,
                                 Lk < Lq, non-finite scale, causal not 0/1,
                                 misaligned pointer */
-  ATTN_ERR_UNSUPPORTED = 2,  /* d_h not 64 or 128, sizes beyond 32-bit tile indexing,
-                                device that is not sm_103 */
+  ATTN_ERR_UNSUPPORTED = 2,  /* d_h not 64 or 128 (128 for fp8), sizes beyond 32-bit
+                                tile indexing, device that is not sm_103 */
   ATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call or the launch failed */
   ATTN_ERR_TIMEOUT = 4       /* a kernel wait ran past its limit (reported by
                                 attn_device_check); outputs of that launch are
@@ -102,6 +102,27 @@ attn_status_t attn_prefill_fwd_chunk(const void* q, const void* k, const void* v
                                      int64_t B, int64_t Lq, int64_t Lk, int32_t n_q,
                                      int32_t n_kv, int32_t d_h, int32_t causal, float scale,
                                      void* stream);
+
+/*
+ * FP8 variant: Q, K and V in e4m3 (OCP FP8 E4M3, 1 byte per element, same
+ * [B, L, H, d_h] layouts) with per-tensor descale factors, so the real inputs
+ * are q*q_descale, k*k_descale, v*v_descale ("prefill-attention" flop record
+ * (phantomic12), "Workarounds": FP8 attention doubles the tensor rate and the
+ * ridge). Both products run on the fp8 tensor cores with fp32 accumulation;
+ * the softmax weights P are rounded to e4m3 for the P.V product (their row
+ * sum stays fp32). O is bf16 and LSE fp32 as above, of the scaled real
+ * scores. Chunks work as in attn_prefill_fwd_chunk (1 <= Lq <= Lk).
+ *
+ *   d_h must be 128 (ATTN_ERR_UNSUPPORTED otherwise); descales must be
+ *   finite (ATTN_ERR_INVALID_ARG otherwise). Everything else as
+ *   attn_prefill_fwd.
+ */
+attn_status_t attn_prefill_fwd_fp8(const void* q, const void* k, const void* v,
+                                   void* o, float* lse,
+                                   int64_t B, int64_t Lq, int64_t Lk, int32_t n_q,
+                                   int32_t n_kv, int32_t d_h, int32_t causal, float scale,
+                                   float q_descale, float k_descale, float v_descale,
+                                   void* stream);
 
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* attn_status_string(attn_status_t status);

@@ -75,3 +75,66 @@ def check_rows(q, k, v, o, lse, rows, causal=True, scale=None, what=""):
     err = errors(o_sel, lse_sel, o_ref, lse_ref)
     assert_within(err, what)
     return err
+
+
+# ----------------------------------------------------------------------------
+# fp8 (e4m3) inputs
+#
+# The oracle runs on the exactly dequantised inputs. The kernel rounds the
+# softmax weights to e4m3 before the P.V product (round to nearest, 3 mantissa
+# bits: relative error <= 2^-4 per weight while the lazy running max keeps
+# every weight <= 2^8, far below the e4m3 limit of 448), keeps their row sum
+# in fp32, and rounds O to bf16. Summed against |V| this bounds each output
+# element by
+#     |O - O_ref| <= 2^-4 * (sum_j p_j |v_j|) / l + 2^-8 |O_ref| + 2^-9,
+# where the first term is the oracle run on |V| and 2^-9 covers weights that
+# fall into the e4m3 subnormal range (absolute error <= 2^-10 each, weighted by
+# values of order 1 over l >= 1). LSE keeps the 1e-3 bar: l is not rounded.
+
+FP8_P_REL = 2.0 ** -4
+
+
+def dequant(t, descale):
+    return t.float().cpu().numpy().astype(np.float64) * float(descale)
+
+
+def fp8_errors(o_gpu, lse_gpu, o_ref, lse_ref, o_abs):
+    d = np.abs(o_gpu - o_ref)
+    bound = FP8_P_REL * o_abs + 2.0 ** -8 * np.abs(o_ref) + 2.0 ** -9
+    return {"o_max_abs": float(d.max()),
+            "o_rel_fro": float(np.linalg.norm(o_gpu - o_ref) / max(np.linalg.norm(o_ref), 1e-30)),
+            "worst_fraction_of_bound": float((d / bound).max()),
+            "lse_max_abs": float(np.abs(lse_gpu - lse_ref).max())}
+
+
+def assert_fp8_within(err, what=""):
+    assert np.isfinite(err["o_max_abs"]) and np.isfinite(err["lse_max_abs"]), (what, err)
+    assert err["worst_fraction_of_bound"] <= 1.0, (what, err)
+    assert err["lse_max_abs"] <= LSE_MAX_ABS, (what, err)
+
+
+def check_fp8_full(q, k, v, o, lse, descales=(1.0, 1.0, 1.0), causal=True, scale=None, what=""):
+    qd, kd, vd = dequant(q, descales[0]), dequant(k, descales[1]), dequant(v, descales[2])
+    o_ref, lse_ref = oracle.attention(qd, kd, vd, causal=causal, scale=scale)
+    o_abs, _ = oracle.attention(qd, kd, np.abs(vd), causal=causal, scale=scale)
+    err = fp8_errors(to_np(o), lse.cpu().numpy().astype(np.float64), o_ref, lse_ref, o_abs)
+    assert_fp8_within(err, what)
+    return err
+
+
+def check_fp8_rows(q, k, v, o, lse, rows, descales=(1.0, 1.0, 1.0), causal=True, scale=None,
+                   what=""):
+    import torch
+
+    n_q = q.shape[2]
+    r = torch.as_tensor(rows, device=q.device)
+    q_sel = dequant(q[r[:, 0], r[:, 2], r[:, 1]], descales[0])
+    kd, vd = dequant(k, descales[1]), dequant(v, descales[2])
+    o_sel = to_np(o[r[:, 0], r[:, 2], r[:, 1]])
+    lse_sel = lse[r[:, 0], r[:, 1], r[:, 2]].cpu().numpy().astype(np.float64)
+    kw = dict(causal=causal, scale=scale, n_q=n_q, lq=q.shape[1])
+    o_ref, lse_ref = oracle.attention_rows(q_sel, kd, vd, rows, **kw)
+    o_abs, _ = oracle.attention_rows(q_sel, kd, np.abs(vd), rows, **kw)
+    err = fp8_errors(o_sel, lse_sel, o_ref, lse_ref, o_abs)
+    assert_fp8_within(err, what)
+    return err

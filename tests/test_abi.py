@@ -94,6 +94,20 @@ def test_chunk_validation(lib, Lq, Lk, expect):
     assert st == expect
 
 
+@pytest.mark.parametrize("args,expect", [
+    (dict(d_h=64), cg.ATTN_ERR_UNSUPPORTED),
+    (dict(qd=math.nan), cg.ATTN_ERR_INVALID_ARG),
+    (dict(vd=math.inf), cg.ATTN_ERR_INVALID_ARG),
+    (dict(q=0), cg.ATTN_ERR_INVALID_ARG),
+])
+def test_fp8_validation(lib, args, expect):
+    a = dict(q=FAKE, d_h=128, qd=1.0, vd=1.0)
+    a.update(args)
+    st = cg.attn_prefill_fwd_fp8(a["q"], FAKE, FAKE, FAKE, FAKE, 1, 128, 128, 4, 2, a["d_h"], 1,
+                                 0.125, a["qd"], 1.0, a["vd"], stream=0)
+    assert st == expect
+
+
 def test_chunk_workload_flops_reduce_to_square():
     w = workloads.custom(1, 300, 4, 2, 64, Lk=300)
     assert w.metric_flops() == oflops.causal_attention_flops(1, 300, 4, 64)
