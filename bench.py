@@ -292,9 +292,17 @@ def run_ours(args, w, dist):
     stream = torch.cuda.current_stream(dev)
     sh = int(stream.cuda_stream)
 
+    ws = None
+    if w.decode:
+        ws = torch.empty(cg.attn_decode_workspace_bytes(w.B, w.keys, w.n_q, w.n_kv, w.d_h),
+                         dtype=torch.uint8, device=dev)
+
     def fwd(q_, k_, v_, o_, l_):
-        # one launch of the C entry point for this workload (chunked when Lk > L)
-        if w.dtype == "e4m3":
+        # one call of the C entry point for this workload (chunked when Lk > L)
+        if w.decode:
+            st = cg.attn_decode_fwd(q_, k_, v_, o_, l_, ws, ws.numel(), w.B, w.keys, w.n_q,
+                                    w.n_kv, w.d_h, w.scale, sh)
+        elif w.dtype == "e4m3":
             st = cg.attn_prefill_fwd_fp8(q_, k_, v_, o_, l_, w.B, w.L, w.keys, w.n_q, w.n_kv,
                                          w.d_h, int(w.causal), w.scale, 1.0, 1.0, 1.0, sh)
         elif w.keys == w.L:
@@ -415,6 +423,15 @@ def run_ours(args, w, dist):
         peak_note += " x 2 (nominal e4m3/bf16 tensor-rate ratio)"
     achieved = flops / (statistics.mean(step_ms) * 1e-3) / 1e12
     traffic = recorded_traffic(w.number)
+    if w.decode:
+        # a decode step is bound by reading the K/V cache once: HBM roofline
+        hbm = float(peaks.get("hbm_gbs", 6800.0))
+        gbs = w.io_bytes() / (statistics.mean(step_ms) * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                "peak_source": f"hbm_gbs ({peak_src})", "traffic": traffic,
+                "algorithmic_bytes_per_launch": w.io_bytes()}
+    else:
+        roof = None
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
@@ -432,9 +449,10 @@ def run_ours(args, w, dist):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "note": "pinned host buffers; uploads, forward and downloads on three streams, "
                         "two device buffer sets, no L2 flush"},
-        "gpu_launches": args.steps,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                     "frac": achieved / peak, "peak_source": peak_note, "traffic": traffic},
+        "gpu_launches": args.steps * (2 if w.decode else 1),
+        "roofline": roof or {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                             "frac": achieved / peak, "peak_source": peak_note,
+                             "traffic": traffic},
         "step_ms_min": min(step_ms), "wall_s_timed": t_wall,
         "grid": cg.attn_prefill_grid_size(w.B, w.L, w.n_q, w.n_kv, w.d_h, w.causal),
     }

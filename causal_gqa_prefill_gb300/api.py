@@ -101,6 +101,54 @@ def attn_prefill_fp8(q, k, v, *, q_descale=1.0, k_descale=1.0, v_descale=1.0, ca
     return out, lse
 
 
+def attn_decode_workspace_bytes(B, Lk, n_q, n_kv, d_h=128) -> int:
+    return int(_abi.load().attn_decode_workspace_bytes(int(B), int(Lk), int(n_q), int(n_kv),
+                                                       int(d_h)))
+
+
+def attn_decode_fwd(q, k, v, o, lse, workspace, workspace_bytes, B, Lk, n_q, n_kv, d_h, scale,
+                    stream=None) -> int:
+    """Direct call of the decode C entry point; returns the raw status code."""
+    lib = _abi.load()
+    return int(lib.attn_decode_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace),
+                                   int(workspace_bytes), int(B), int(Lk), int(n_q), int(n_kv),
+                                   int(d_h), float(scale), _stream_handle(stream)))
+
+
+def attn_decode(q, k, v, *, scale=None, workspace=None, out=None, lse=None, stream=None):
+    """One decode step: q bf16 [B, 1, n_q, 128] against the cache k/v bf16
+    [B, Lk, n_kv, 128]. Returns (o bf16 [B, 1, n_q, 128], lse fp32 [B, n_q, 1]).
+    ``workspace`` (a CUDA tensor of at least attn_decode_workspace_bytes
+    bytes) is allocated with torch when not given."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be a bfloat16 CUDA tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B, L, H, d_h] tensor")
+    B, one, n_q, d = q.shape
+    if one != 1 or k.shape != v.shape or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("q must be [B, 1, n_q, d_h] and k, v [B, Lk, n_kv, d_h]")
+    Lk, n_kv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = attn_decode_workspace_bytes(B, Lk, n_q, n_kv, d)
+    if need < 0:
+        raise AttnError(_abi.ATTN_ERR_UNSUPPORTED, "attn_decode_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, n_q, 1), dtype=torch.float32, device=q.device)
+    nbytes = workspace.numel() * workspace.element_size()
+    st = attn_decode_fwd(q, k, v, out, lse, workspace, nbytes, B, Lk, n_q, n_kv, d, scale, stream)
+    if st != _abi.ATTN_OK:
+        raise AttnError(st, "attn_decode_fwd")
+    return out, lse
+
+
 def attn_device_check(stream=None) -> int:
     """Synchronise the stream and report device-side timeouts (raw status)."""
     return int(_abi.load().attn_device_check(_stream_handle(stream)))

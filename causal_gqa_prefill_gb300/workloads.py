@@ -30,6 +30,7 @@ class Workload:
     full_check: bool = True         # oracle over every row (else sampled rows)
     Lk: int = 0                     # keys (0: = L); L < Lk makes Q the last L positions
     dtype: str = "bf16"             # "bf16" or "e4m3" (Q, K, V stored as fp8, descale 1)
+    decode: bool = False            # one query token per sequence against Lk cached keys
 
     @property
     def keys(self) -> int:
@@ -58,7 +59,7 @@ class Workload:
         way, 4*d_h*(offset + i) per row i summed in the L^2/2 form:
         2*n_q*d_h*(2*L*offset + L^2)*B (equal to the square count at offset 0).
         """
-        if not self.causal:
+        if self.decode or not self.causal:
             return 4 * self.n_q * self.d_h * self.L * self.keys * self.B
         return 2 * self.n_q * self.d_h * (2 * self.L * self.offset + self.L * self.L) * self.B
 
@@ -75,6 +76,8 @@ class Workload:
             d["Lk"] = self.keys
         if self.dtype != "bf16":
             d["inputs"] = self.dtype
+        if self.decode:
+            d["step"] = "decode"
         return d
 
 
@@ -101,6 +104,12 @@ WORKLOADS = {
                    "d_h=128)", 1, 8192, 32, 8, 128, dtype="e4m3", full_check=False),
     9: Workload(9, "fp8 e4m3, long-context 36-head shape, GQA-6 (B=1, L=131072, n_q=36, n_kv=6, "
                    "d_h=128)", 1, 131072, 36, 6, 128, dtype="e4m3", full_check=False),
+    # decode: one new token per sequence against its cache
+    10: Workload(10, "decode, Llama-3-8B-shaped layer: 16 sequences with 8192 cached tokens "
+                     "(B=16, Lk=8192, n_q=32, n_kv=8, d_h=128)", 16, 1, 32, 8, 128, Lk=8192,
+                 decode=True),
+    11: Workload(11, "decode, 36-head shape after a 131072-token prompt (B=1, Lk=131072, n_q=36, "
+                     "n_kv=6, d_h=128)", 1, 1, 36, 6, 128, Lk=131072, decode=True),
 }
 
 

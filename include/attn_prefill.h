@@ -124,6 +124,31 @@ attn_status_t attn_prefill_fwd_fp8(const void* q, const void* k, const void* v,
                                    float q_descale, float k_descale, float v_descale,
                                    void* stream);
 
+/*
+ * Decode attention: one new query token per sequence attends to its whole
+ * key/value cache ("Long-Context Attention Explained" (sevydevy), prefill vs
+ * decode: decode has one new query per step and reads every cached key and
+ * value). It is attn_prefill_fwd_chunk with Lq = 1 (the token sits at
+ * position Lk - 1, so it sees keys 0..Lk-1), computed by a kernel built for
+ * a memory-bound step: the key range is split over many CTAs that stream K
+ * and V once, and a second kernel merges the partial results.
+ *
+ *   q    bf16 [B, 1, n_q, 128]           k, v  bf16 [B, Lk, n_kv, 128]
+ *   o    bf16 [B, 1, n_q, 128]           lse   fp32 [B, n_q, 1]
+ *   workspace  device memory of at least attn_decode_workspace_bytes(...)
+ *              bytes, 16-byte aligned, owned by the caller; its contents
+ *              on entry are ignored and on exit unspecified.
+ *   n_q / n_kv <= 8 and d_h = 128 (ATTN_ERR_UNSUPPORTED otherwise); a NULL
+ *   or too-small workspace is ATTN_ERR_INVALID_ARG. Everything else as
+ *   attn_prefill_fwd.
+ */
+int64_t attn_decode_workspace_bytes(int64_t B, int64_t Lk, int32_t n_q, int32_t n_kv,
+                                    int32_t d_h);   /* -1 on invalid or unsupported sizes */
+attn_status_t attn_decode_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                              void* workspace, int64_t workspace_bytes,
+                              int64_t B, int64_t Lk, int32_t n_q, int32_t n_kv, int32_t d_h,
+                              float scale, void* stream);
+
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* attn_status_string(attn_status_t status);
 

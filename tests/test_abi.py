@@ -108,6 +108,22 @@ def test_fp8_validation(lib, args, expect):
     assert st == expect
 
 
+def test_decode_workspace_and_validation(lib):
+    assert cg.attn_decode_workspace_bytes(1, 1000, 8, 2) > 0
+    assert cg.attn_decode_workspace_bytes(1, 1000, 8, 2, 64) == -1
+    assert cg.attn_decode_workspace_bytes(0, 1000, 8, 2) == -1
+    need = cg.attn_decode_workspace_bytes(1, 1000, 8, 2)
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, need, 1, 1000, 8, 2, 128, 0.1]
+    bad = list(args); bad[5] = 0                       # no workspace
+    assert cg.attn_decode_fwd(*bad, stream=0) == cg.ATTN_ERR_INVALID_ARG
+    bad = list(args); bad[6] = need - 16               # workspace too small
+    assert cg.attn_decode_fwd(*bad, stream=0) == cg.ATTN_ERR_INVALID_ARG
+    bad = list(args); bad[11] = 64                     # head dim
+    assert cg.attn_decode_fwd(*bad, stream=0) == cg.ATTN_ERR_UNSUPPORTED
+    bad = list(args); bad[9], bad[10] = 18, 2          # g = 9
+    assert cg.attn_decode_fwd(*bad, stream=0) == cg.ATTN_ERR_UNSUPPORTED
+
+
 def test_chunk_workload_flops_reduce_to_square():
     w = workloads.custom(1, 300, 4, 2, 64, Lk=300)
     assert w.metric_flops() == oflops.causal_attention_flops(1, 300, 4, 64)

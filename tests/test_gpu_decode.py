@@ -1,0 +1,93 @@
+"""GPU parity of the decode kernel (one new token per sequence against its
+cache) against the fp64 oracle: the chunked definition with Lq = 1."""
+
+import numpy as np
+import pytest
+
+from causal_gqa_prefill_gb300 import (ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_OK,
+                                      attn_decode, attn_decode_fwd, attn_decode_workspace_bytes,
+                                      attn_device_check, attn_prefill)
+from causal_gqa_prefill_gb300 import workloads as W
+from gpu_common import check_full
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from causal_gqa_prefill_gb300 import build
+    build.build()
+    torch.cuda.set_device(0)
+
+
+def _decode(q, k, v, **kw):
+    o, lse = attn_decode(q, k, v, **kw)
+    assert attn_device_check() == ATTN_OK
+    return o, lse
+
+
+DECODE = [
+    # B, Lk, n_q, n_kv
+    (2, 1000, 8, 2),
+    (1, 1, 4, 1),          # a single cached key
+    (3, 300, 6, 2),        # g = 3
+    (4, 777, 4, 4),        # g = 1
+    (1, 2049, 8, 1),       # g = 8, ragged last tile
+    (1, 5000, 32, 8),
+    (2, 64, 2, 2),         # exactly one tile
+]
+
+
+@pytest.mark.parametrize("case", DECODE, ids=lambda c: "B%d_Lk%d_q%d_kv%d" % c)
+def test_decode_small_shapes(case):
+    B, Lk, n_q, n_kv = case
+    w = W.custom(B, 1, n_q, n_kv, 128, Lk=Lk)
+    q, k, v = W.make_inputs(w, "cuda", seed=hash(case) % 100000)
+    o, lse = _decode(q, k, v)
+    check_full(q, k, v, o, lse, what=str(case))
+
+
+def test_decode_matches_last_row_of_prefill():
+    """The decode step equals the last row of a causal prefill over the whole
+    sequence (same keys, same query)."""
+    w = W.custom(2, 3000, 8, 2, 128)
+    qf, k, v = W.make_inputs(w, "cuda", seed=11)
+    o_full, l_full = attn_prefill(qf, k, v)
+    o, lse = _decode(qf[:, -1:].contiguous(), k, v)
+    assert (o.float() - o_full[:, -1:].float()).abs().max().item() <= 1e-2
+    assert (lse - l_full[:, :, -1:]).abs().max().item() <= 1e-3
+
+
+def test_decode_workspace_is_reused():
+    w1 = W.custom(2, 1, 8, 2, 128, Lk=1500)
+    ws = torch.empty(attn_decode_workspace_bytes(2, 1500, 8, 2), dtype=torch.uint8, device="cuda")
+    for seed in (1, 2):
+        q, k, v = W.make_inputs(w1, "cuda", seed=seed)
+        o, lse = _decode(q, k, v, workspace=ws)
+        check_full(q, k, v, o, lse, what=f"reuse {seed}")
+
+
+@pytest.mark.parametrize("num", [10, 11])
+def test_decode_workloads(num):
+    w = W.WORKLOADS[num]
+    q, k, v = W.make_inputs(w, "cuda")
+    o, lse = _decode(q, k, v, scale=w.scale)
+    err = check_full(q, k, v, o, lse, scale=w.scale, what=w.name)
+    print(f"parity {w.name}: {err}")
+
+
+def test_decode_argument_errors():
+    q = torch.zeros(1, 1, 16, 128, device="cuda", dtype=torch.bfloat16)
+    kv = torch.zeros(1, 64, 1, 128, device="cuda", dtype=torch.bfloat16)
+    o = torch.empty_like(q)
+    lse = torch.empty(1, 16, 1, device="cuda")
+    ws = torch.empty(1 << 16, dtype=torch.uint8, device="cuda")
+    assert attn_decode_fwd(q, kv, kv, o, lse, ws, ws.numel(), 1, 64, 16, 1, 128, 0.1) == \
+        ATTN_ERR_UNSUPPORTED                                  # g = 16 > 8
+    q = torch.zeros(1, 1, 8, 128, device="cuda", dtype=torch.bfloat16)
+    need = attn_decode_workspace_bytes(1, 64, 8, 1)
+    assert attn_decode_fwd(q, kv, kv, torch.empty_like(q), lse, ws, need - 1, 1, 64, 8, 1, 128,
+                           0.1) == ATTN_ERR_INVALID_ARG        # workspace too small
