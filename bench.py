@@ -213,6 +213,35 @@ def oracle_sample(w, q_host, k_host, v_host, rng, rows_per_chunk, seconds=None, 
     return flops, spent, nrows
 
 
+def oracle_backward_sample(w, q_host, k_host, v_host, do_host, rng, rows, seconds=None,
+                           calls=None):
+    """Times the fp64 backward oracle on causal prefixes of ``rows`` positions of
+    random (batch, K/V head) groups; returns (flops, seconds, calls). A prefix
+    of a causal problem is a complete smaller problem; its metric count is
+    2.5 x the forward's 2*g*d_h*rows^2."""
+    import oracle
+
+    flops, spent, done = 0.0, 0.0, 0
+    g = w.g
+    while True:
+        b = int(rng.integers(0, w.B))
+        kvh = int(rng.integers(0, w.n_kv))
+        hs = slice(kvh * g, (kvh + 1) * g)
+        args = (q_host[b:b + 1, :rows, hs], k_host[b:b + 1, :rows, kvh:kvh + 1],
+                v_host[b:b + 1, :rows, kvh:kvh + 1], do_host[b:b + 1, :rows, hs])
+        t0 = time.perf_counter()
+        oracle.attention_backward(*args, causal=w.causal, scale=w.scale)
+        spent += time.perf_counter() - t0
+        per = 2 * g * w.d_h * rows * rows * (1 if w.causal else 2)
+        flops += per * 5 / 2
+        done += 1
+        if seconds is not None and spent >= seconds:
+            break
+        if calls is not None and done >= calls:
+            break
+    return flops, spent, done
+
+
 def blas_threads() -> int:
     try:
         from threadpoolctl import threadpool_info
@@ -234,6 +263,8 @@ def host_inputs(w):
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     q, k, v = W.make_inputs(w, dev)
     f = lambda t: t.float().cpu().numpy().astype(np.float64)
+    if w.backward:
+        return f(q), f(k), f(v), f(W.make_grad(w, dev))
     return f(q), f(k), f(v)
 
 
@@ -242,6 +273,8 @@ def run_reference(args, w, dist):
 
     if dist.rank != 0:
         return 0
+    if w.backward:
+        return run_reference_backward(args, w)
     q, k, v = host_inputs(w)
     rng = np.random.default_rng(w.seed)
     # Size each step so that warm-up plus timed steps take about
@@ -269,6 +302,49 @@ def run_reference(args, w, dist):
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{rows_per_step} random query rows per step of {w.name}; "
                                    "fp64 NumPy oracle on the host cores"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def backward_prefix_rows(w, q, k, v, do, rng, target_s):
+    """Prefix length whose backward oracle call takes about ``target_s`` seconds."""
+    rows = min(w.L, 512)
+    while True:
+        _, s, _ = oracle_backward_sample(w, q, k, v, do, rng, rows, calls=1)
+        if s >= target_s or rows >= w.L:
+            return rows
+        rows = min(w.L, int(rows * max(1.25, min(4.0, (target_s / max(s, 1e-6)) ** 0.5))))
+        rows = max(128, rows // 128 * 128)
+
+
+def run_reference_backward(args, w):
+    import numpy as np
+
+    q, k, v, do = host_inputs(w)
+    rng = np.random.default_rng(w.seed)
+    budget = args.ref_seconds / (args.steps + args.warmup)
+    rows = backward_prefix_rows(w, q, k, v, do, rng, budget)
+    for _ in range(args.warmup):
+        oracle_backward_sample(w, q, k, v, do, rng, rows, calls=1)
+    total_flops, total_s, step_ms = 0.0, 0.0, []
+    for _ in range(args.steps):
+        f, s, _ = oracle_backward_sample(w, q, k, v, do, rng, rows, calls=1)
+        total_flops += f
+        total_s += s
+        step_ms.append(s * 1e3)
+    value = total_flops / total_s / 1e12
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(step_ms),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": dict(w.describe()),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"backward of the first {rows} positions of one random "
+                                   f"(batch, K/V head) group per step of {w.name}; fp64 NumPy "
+                                   "oracle on the host cores"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -314,8 +390,26 @@ def run_ours(args, w, dist):
         if st != cg.ATTN_OK:
             raise cg.AttnError(st, "attention forward")
 
-    def step():
+    bwd_ws = dout = grads = None
+    if w.backward:
+        # the forward's outputs are inputs of the backward step: computed once here
         fwd(q, k, v, o, lse)
+        dout = W.make_grad(w, dev)
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+        bwd_ws = torch.empty(cg.attn_prefill_bwd_workspace_bytes(w.B, w.L, w.n_q, w.n_kv, w.d_h),
+                             dtype=torch.uint8, device=dev)
+
+    def bwd(q_, k_, v_, o_, l_, do_, dq_, dk_, dv_):
+        st = cg.attn_prefill_bwd(q_, k_, v_, o_, l_, do_, dq_, dk_, dv_, bwd_ws, bwd_ws.numel(),
+                                 w.B, w.L, w.n_q, w.n_kv, w.d_h, int(w.causal), w.scale, sh)
+        if st != cg.ATTN_OK:
+            raise cg.AttnError(st, "attention backward")
+
+    def step():
+        if w.backward:
+            bwd(q, k, v, o, lse, dout, *grads)
+        else:
+            fwd(q, k, v, o, lse)
 
     sampler = ClockSampler(dist.local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
     sampler.start()
@@ -351,19 +445,25 @@ def run_ours(args, w, dist):
     value = dist.world * flops / (mean_ms * 1e-3) / 1e12
 
     # End to end through the public API: every step copies its inputs from
-    # pinned host memory and its outputs (O and LSE) back to pinned host
-    # memory. Copies run on their own streams with two device buffer sets, so
-    # step i+1's upload and step i-1's download overlap step i's forward (a
-    # pipelined serving loop); the timed region spans all K steps' copies.
-    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
-    ho = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for _ in range(2)]
-    hl = [torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True) for _ in range(2)]
-    dq = [q, q.clone()]
-    dk = [k, k.clone()]
-    dv = [v, v.clone()]
-    do_ = [o, torch.empty_like(o)]
-    dl = [lse, torch.empty_like(lse)]
+    # pinned host memory and its outputs back to pinned host memory (forward:
+    # Q, K, V in, O and LSE out; backward: Q, K, V, O, LSE, dO in, dQ, dK, dV
+    # out). Copies run on their own streams with two device buffer sets, so
+    # step i+1's upload and step i-1's download overlap step i's compute (a
+    # pipelined loop); the timed region spans all K steps' copies.
+    dev_in = [q, k, v] + ([o, lse, dout] if w.backward else [])
+    dev_out = list(grads) if w.backward else [o, lse]
+    host_in = [t.cpu().pin_memory() for t in dev_in]
+    host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_out]
+                for _ in range(2)]
+    bufs_in = [dev_in, [t.clone() for t in dev_in]]
+    bufs_out = [dev_out, [torch.empty_like(t) for t in dev_out]]
     s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def call(b):
+        if w.backward:
+            bwd(*bufs_in[b], *bufs_out[b])
+        else:
+            fwd(*bufs_in[b], *bufs_out[b])
 
     def e2e_run(nsteps):
         ev_up = [torch.cuda.Event() for _ in range(nsteps)]
@@ -374,19 +474,18 @@ def run_ours(args, w, dist):
             with torch.cuda.stream(s_up):
                 if i >= 2:
                     s_up.wait_event(ev_fw[i - 2])
-                dq[b].copy_(hq, non_blocking=True)
-                dk[b].copy_(hk, non_blocking=True)
-                dv[b].copy_(hv, non_blocking=True)
+                for d_, h_ in zip(bufs_in[b], host_in):
+                    d_.copy_(h_, non_blocking=True)
                 ev_up[i].record(s_up)
             stream.wait_event(ev_up[i])
             if i >= 2:
                 stream.wait_event(ev_dn[i - 2])
-            fwd(dq[b], dk[b], dv[b], do_[b], dl[b])
+            call(b)
             ev_fw[i].record(stream)
             with torch.cuda.stream(s_down):
                 s_down.wait_event(ev_fw[i])
-                ho[b].copy_(do_[b], non_blocking=True)
-                hl[b].copy_(dl[b], non_blocking=True)
+                for h_, d_ in zip(host_out[b], bufs_out[b]):
+                    h_.copy_(d_, non_blocking=True)
                 ev_dn[i].record(s_down)
         stream.wait_event(ev_dn[nsteps - 1])
 
@@ -401,8 +500,8 @@ def run_ours(args, w, dist):
     torch.cuda.synchronize()
     dist.barrier()
     e2e_ms = dist.max(e_start.elapsed_time(e_end) / args.steps)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-    d2h = ho[0].numel() * ho[0].element_size() + hl[0].numel() * hl[0].element_size()
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
     e2e_value = dist.world * flops / (e2e_ms * 1e-3) / 1e12
 
     peaks, peak_src = measured_peaks()
@@ -430,6 +529,11 @@ def run_ours(args, w, dist):
         roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                 "peak_source": f"hbm_gbs ({peak_src})", "traffic": traffic,
                 "algorithmic_bytes_per_launch": w.io_bytes()}
+    elif w.backward:
+        # the step is three launches (row statistics, dK/dV, dQ): timed as one
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                "frac": achieved / peak, "peak_source": peak_note, "traffic": traffic,
+                "kernel": "backward step (rowdot + dkdv + dq launches), 2.5x forward FLOPs"}
     else:
         roof = None
     line = {
@@ -439,6 +543,8 @@ def run_ours(args, w, dist):
         "dtype": "e4m3" if w.dtype == "e4m3" else "bf16",
         "data": "synthetic",
         "config": dict(w.describe(), parallelism=f"replicas x{dist.world}",
+                       **({"flop_count": "2.5 x 2*n_q*d_h*L^2*B (five products of the forward's "
+                                         "size against two)"} if w.backward else {}),
                        l2="flushed before every step (256 MiB device write, outside the timed interval)"),
         "pct_of_peak": 100.0 * achieved / peak,
         "pct_of_burst": 100.0 * achieved / burst,
@@ -447,16 +553,25 @@ def run_ours(args, w, dist):
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "note": "pinned host buffers; uploads, forward and downloads on three streams, "
+                "note": "pinned host buffers; uploads, compute and downloads on three streams, "
                         "two device buffer sets, no L2 flush"},
-        "gpu_launches": args.steps * (2 if w.decode else 1),
+        "gpu_launches": args.steps * (2 if w.decode else 3 if w.backward else 1),
         "roofline": roof or {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                              "frac": achieved / peak, "peak_source": peak_note,
                              "traffic": traffic},
         "step_ms_min": min(step_ms), "wall_s_timed": t_wall,
         "grid": cg.attn_prefill_grid_size(w.B, w.L, w.n_q, w.n_kv, w.d_h, w.causal),
     }
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline and w.backward:
+        fq, fk, fv, fd = (t.float().cpu().numpy().astype(np.float64) for t in (q, k, v, dout))
+        rng = np.random.default_rng(w.seed)
+        rows = backward_prefix_rows(w, fq, fk, fv, fd, rng, args.cpu_seconds / 4)
+        f, s, n = oracle_backward_sample(w, fq, fk, fv, fd, rng, rows, seconds=args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": f / s / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"backward of the first {rows} positions of {n} random (batch, K/V head) "
+                      f"groups of {w.name} (fp64 NumPy oracle), {s:.1f} s"}
+    elif dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         fq, fk, fv = (t.float().cpu().numpy().astype(np.float64) for t in (q, k, v))
         rng = np.random.default_rng(w.seed)
         f, s, n = oracle_sample(w, fq, fk, fv, rng, 256, seconds=args.cpu_seconds)

@@ -1,4 +1,4 @@
-"""GB300-native causal GQA prefill attention (forward).
+"""GB300-native causal GQA prefill attention (forward, decode and backward).
 
 The computation runs in a hand-written sm_103a CUDA library
 (``lib/libattn_prefill.so``, C ABI in ``include/attn_prefill.h``); this
@@ -10,12 +10,14 @@ from ._abi import (ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR
                    ATTN_ERR_TIMEOUT, load as load_library, library_path, status_string)
 from .api import (AttnError, attn_decode, attn_decode_fwd, attn_decode_workspace_bytes,
                   attn_prefill, attn_prefill_fp8, attn_prefill_fwd, attn_prefill_fwd_chunk,
-                  attn_prefill_fwd_fp8, attn_device_check, attn_prefill_grid_size)
+                  attn_prefill_fwd_fp8, attn_device_check, attn_prefill_grid_size,
+                  attn_prefill_backward, attn_prefill_bwd, attn_prefill_bwd_workspace_bytes)
 
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_CUDA",
     "ATTN_ERR_TIMEOUT", "AttnError", "attn_prefill", "attn_prefill_fwd", "attn_prefill_fwd_chunk",
     "attn_prefill_fp8", "attn_prefill_fwd_fp8", "attn_decode", "attn_decode_fwd",
-    "attn_decode_workspace_bytes", "attn_device_check",
+    "attn_decode_workspace_bytes", "attn_device_check", "attn_prefill_backward",
+    "attn_prefill_bwd", "attn_prefill_bwd_workspace_bytes",
     "attn_prefill_grid_size", "load_library", "library_path", "status_string",
 ]

@@ -1,6 +1,6 @@
 """ctypes binding of the C ABI declared in include/attn_prefill.h.
 
-Argument marshalling only: every step of the attention forward runs in the
+Argument marshalling only: every step of the attention passes runs in the
 CUDA library. There is no CPU fallback; a missing library raises.
 """
 
@@ -49,6 +49,16 @@ _SIGNATURES = {
                                        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                        ctypes.c_float, ctypes.c_void_p]),
+    "attn_prefill_bwd_workspace_bytes": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int64,
+                                                          ctypes.c_int32, ctypes.c_int32,
+                                                          ctypes.c_int32]),
+    "attn_prefill_bwd": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_int64,
+                                        ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                        ctypes.c_float, ctypes.c_void_p]),
     "attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_device_check": (ctypes.c_int, [ctypes.c_void_p]),
     "attn_prefill_grid_size": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,

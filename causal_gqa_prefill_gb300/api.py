@@ -149,6 +149,63 @@ def attn_decode(q, k, v, *, scale=None, workspace=None, out=None, lse=None, stre
     return out, lse
 
 
+def attn_prefill_bwd_workspace_bytes(B, L, n_q, n_kv, d_h=128) -> int:
+    return int(_abi.load().attn_prefill_bwd_workspace_bytes(int(B), int(L), int(n_q), int(n_kv),
+                                                            int(d_h)))
+
+
+def attn_prefill_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, L, n_q,
+                     n_kv, d_h, causal, scale, stream=None) -> int:
+    """Direct call of the backward C entry point; returns the raw status code."""
+    lib = _abi.load()
+    return int(lib.attn_prefill_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                                    _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                                    int(workspace_bytes), int(B), int(L), int(n_q), int(n_kv),
+                                    int(d_h), int(causal), float(scale), _stream_handle(stream)))
+
+
+def attn_prefill_backward(q, k, v, o, lse, dout, *, causal=True, scale=None, workspace=None,
+                          dq=None, dk=None, dv=None, stream=None):
+    """Gradients (dq, dk, dv) of attn_prefill for the upstream gradient ``dout``.
+
+    q, o, dout: bf16 CUDA tensors [B, L, n_q, 128]; k, v: [B, L, n_kv, 128];
+    lse: the forward's fp32 [B, n_q, L]. Outputs are allocated unless passed
+    in; ``workspace`` (at least attn_prefill_bwd_workspace_bytes bytes) is
+    allocated with torch when not given."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be a bfloat16 CUDA tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B, L, H, d_h] tensor")
+    B, L, n_q, d = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[1] != L or k.shape[3] != d:
+        raise ValueError("k and v must be [B, L, n_kv, d_h] matching q")
+    if o.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("o and dout must be shaped like q")
+    n_kv = k.shape[2]
+    if (not isinstance(lse, torch.Tensor) or lse.dtype != torch.float32 or not lse.is_cuda
+            or tuple(lse.shape) != (B, n_q, L) or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 CUDA tensor [B, n_q, L]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = attn_prefill_bwd_workspace_bytes(B, L, n_q, n_kv, d)
+    if need < 0:
+        raise AttnError(_abi.ATTN_ERR_UNSUPPORTED, "attn_prefill_bwd_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    nbytes = workspace.numel() * workspace.element_size()
+    st = attn_prefill_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, nbytes, B, L, n_q, n_kv,
+                          d, int(bool(causal)), scale, stream)
+    if st != _abi.ATTN_OK:
+        raise AttnError(st, "attn_prefill_bwd")
+    return dq, dk, dv
+
+
 def attn_device_check(stream=None) -> int:
     """Synchronise the stream and report device-side timeouts (raw status)."""
     return int(_abi.load().attn_device_check(_stream_handle(stream)))

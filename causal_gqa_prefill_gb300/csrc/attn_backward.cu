@@ -1,0 +1,612 @@
+// attn_backward.cu — gradients of the causal GQA attention forward on GB300
+// (sm_103a), by recomputation from the saved log-sum-exp.
+//
+// The backward pass rebuilds each score tile from Q, K and the forward's row
+// statistics instead of storing the L x L table ("Long-Context Attention
+// Explained" (sevydevy), "What FlashAttention does not change"). With
+// P = exp(scale*S - LSE), D_i = dO_i . O_i:
+//
+//   dV_j = sum_i P_ij dO_i        dP = dO V^T        dS = P * (dP - D)
+//   dK_j = scale sum_i dS_ij Q_i  dQ_i = scale sum_j dS_ij K_j
+//
+// Three kernels, no atomics:
+//   rowdot  per query row: LSE*log2(e) and D = dO . O, padded to whole
+//           128-row tiles (+inf / 0) so tiles can be fetched with bulk copies;
+//   dkdv    one CTA per (b, K/V head, 128-key tile j): loops over the g query
+//           heads of the group and the query tiles that see tile j; with the
+//           key dimension on the TMEM lanes it computes S^T = K Q^T and
+//           dP^T = V dO^T (tcgen05, both operands from shared memory), turns
+//           them into P^T and dS^T (bf16, written back into TMEM) and
+//           accumulates dV += P^T dO and dK += dS^T Q (A from TMEM); dK and dV
+//           for the whole group stay in TMEM until the end;
+//   dq      one CTA per (b, query head, 128-row tile i): S = Q K^T and
+//           dP = dO V^T, dS in TMEM, dQ += dS K over the key tiles it sees.
+// Each kernel has a TMA producer warp, an MMA warp (warp-wide loop, one elected
+// issuing lane) and a 128-thread compute warpgroup (thread = TMEM lane).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn_prefill.h"
+#include "sm103_ptx.cuh"
+
+namespace gb300_host {
+attn_status_t device_status_word(cudaStream_t stream, int** status);
+}
+
+namespace {
+
+using namespace gb300;
+
+constexpr int kD = 128;                  // head dimension
+constexpr int kT = 128;                  // rows per query tile and keys per key tile
+constexpr int kTileBytes = kT * kD * 2;  // one bf16 128 x 128 tile (two 64-column chunks)
+constexpr int kThreads = 192;            // warps 0-3 compute, 4 producer, 5 MMA
+constexpr int kLoadWarp = 4, kMmaWarp = 5;
+constexpr long long kSpinLimit = 1ll << 31;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct BwdParams {
+  int L, n_q, n_kv, g, T;   // T = 128-row tiles per sequence
+  int causal;
+  float c;                  // scale * log2(e)
+  float scale;
+  const float* lse2;        // [B, n_q, T*128] LSE * log2(e), +inf past L
+  const float* rowdot;      // [B, n_q, T*128] D, 0 past L
+  uint16_t* dq;             // bf16 [B, L, n_q, 128]
+  uint16_t* dk;             // bf16 [B, L, n_kv, 128]
+  uint16_t* dv;
+  int* status;
+};
+
+struct Sync {
+  uint64_t fixed_full;              // the CTA's fixed tiles (K_j, V_j or Q_i, dO_i)
+  uint64_t full[2], empty[2];       // two-stage ring of streamed tiles
+  uint64_t s_full, p_full, done, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, Sync& sy,
+                                             const BwdParams& p) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = clock64_now();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*reinterpret_cast<volatile int*>(&sy.abort)) return false;
+    if (static_cast<long long>(clock64_now() - t0) > kSpinLimit) {
+      *reinterpret_cast<volatile int*>(&sy.abort) = 1;
+      atomicOr(p.status, 1);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = clock64_now();
+  while (!mbar_try_wait(bar, parity))
+    if (static_cast<long long>(clock64_now() - t0) > kSpinLimit) return;
+}
+
+// Plain (non-tensor) bulk copy global -> shared, completion on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+        "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
+        "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// 128x128x128 product into TMEM, A and B [128 rows x 128] K-major bf16 tiles.
+__device__ __forceinline__ void mma_rows_x_rows(bool leader, uint32_t d_tmem, uint32_t a_smem,
+                                                uint32_t b_smem) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kT, kT, false);
+#pragma unroll
+  for (int kk = 0; kk < kD / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * (kT * 128) + (kk & 3) * 32;
+    const uint64_t a = sdesc_sw128(a_smem + off, 16, 1024);
+    const uint64_t b = sdesc_sw128(b_smem + off, 16, 1024);
+    if (leader) mma_ss(d_tmem, a, b, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// D[tmem] (+)= A[tmem] (128 x 128, bf16 packed two per column) * B, where B is
+// a [128 rows x 128] bf16 tile used MN-major (its rows are the K dimension).
+__device__ __forceinline__ void mma_tmem_x_rows(bool leader, uint32_t d_tmem, uint32_t a_tmem,
+                                                uint32_t b_smem, bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kT, kD, true);
+#pragma unroll
+  for (int kk = 0; kk < kT / 16; ++kk) {
+    const uint64_t b = sdesc_sw128(b_smem + kk * 16 * 128, kT * 128, 1024);
+    if (leader) mma_ts(d_tmem, a_tmem + kk * 8, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+__device__ __forceinline__ void setup(Sync& sy, int nfull) {
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&sy.fixed_full), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_addr(&sy.full[s]), 1);
+      mbar_init(smem_addr(&sy.empty[s]), 1);
+    }
+    mbar_init(smem_addr(&sy.s_full), 1);
+    mbar_init(smem_addr(&sy.p_full), nfull);
+    mbar_init(smem_addr(&sy.done), 1);
+    mbar_init(smem_addr(&sy.drain), 1);
+    sy.abort = 0;
+    fence_mbar_init();
+  }
+  if ((threadIdx.x >> 5) == kMmaWarp) {
+    tmem_alloc(smem_addr(&sy.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+}
+
+__device__ __forceinline__ void teardown(Sync& sy, const BwdParams& p, bool leader_mma) {
+  if ((threadIdx.x >> 5) == kMmaWarp) {
+    if (leader_mma) mma_commit(smem_addr(&sy.drain));
+    wait_drain(smem_addr(&sy.drain), 0);
+    __syncwarp();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if ((threadIdx.x >> 5) == kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(sy.tmem_base, 512);
+  }
+}
+
+// bf16 output row (128 values) from 4 x 32 fp32 TMEM columns, times `mul`.
+__device__ __forceinline__ void store_row(uint32_t t_row, uint16_t* dst, float mul, bool valid) {
+#pragma unroll 1
+  for (int c = 0; c < kD; c += 32) {
+    uint32_t v[32];
+    tmem_ld32(t_row + c, v);
+    tmem_wait_ld(v);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      w[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+    if (valid) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ rowdot
+
+__global__ void rowdot_kernel(const uint16_t* o, const uint16_t* dout, const float* lse,
+                              float* lse2, float* rowdot, int B, int L, int n_q, int Lp) {
+  // one warp per padded row (b, h, t); t < Lp
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int64_t total = static_cast<int64_t>(B) * n_q * Lp;
+  if (row >= total) return;
+  const int t = static_cast<int>(row % Lp);
+  const int64_t bh = row / Lp;
+  const int h = static_cast<int>(bh % n_q);
+  const int b = static_cast<int>(bh / n_q);
+  float dd = 0.0f;
+  if (t < L) {
+    const size_t off = ((static_cast<size_t>(b) * L + t) * n_q + h) * kD + 4 * lane;
+    const uint2 a = *reinterpret_cast<const uint2*>(o + off);
+    const uint2 d = *reinterpret_cast<const uint2*>(dout + off);
+    dd = __uint_as_float(a.x << 16) * __uint_as_float(d.x << 16) +
+         __uint_as_float(a.x & 0xFFFF0000u) * __uint_as_float(d.x & 0xFFFF0000u) +
+         __uint_as_float(a.y << 16) * __uint_as_float(d.y << 16) +
+         __uint_as_float(a.y & 0xFFFF0000u) * __uint_as_float(d.y & 0xFFFF0000u);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, off);
+  if (lane == 0) {
+    rowdot[row] = dd;
+    lse2[row] = (t < L) ? lse[bh * L + t] * kLog2e : INFINITY;
+  }
+}
+
+// -------------------------------------------------------------------- dK, dV
+
+__global__ void __launch_bounds__(kThreads, 1)
+dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+            const BwdParams p) {
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ Sync sy;
+  // smem: K_j | V_j | stage 0: Q, dO, lse2[128], D[128] | stage 1: same
+  const uint32_t base = (smem_addr(dyn_smem) + 1023u) & ~1023u;
+  const uint32_t sK = base, sV = base + kTileBytes;
+  constexpr uint32_t kStage = 2 * kTileBytes + 1024;
+  const uint32_t sStage = base + 2 * kTileBytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int groups = static_cast<int>(gridDim.x) / p.T;
+  const int j = blockIdx.x / groups;                  // key tile (ascending = most work first)
+  const int grp = blockIdx.x - j * groups;
+  const int b = grp / p.n_kv, kvh = grp - b * p.n_kv;
+  const int i0 = p.causal ? j : 0;
+  const int nsteps = p.g * (p.T - i0);                 // (head, query tile) pairs
+  setup(sy, 128);
+  const uint32_t tmem = sy.tmem_base;
+
+  if (warp == kLoadWarp) {
+    if (lane == 0) {
+      const uint32_t fb = smem_addr(&sy.fixed_full);
+      mbar_arrive_expect_tx(fb, 2 * kTileBytes);
+      for (int c = 0; c < 2; ++c) {
+        tma_load_4d(sK + c * kT * 128, &tmK, fb, c * 64, kvh, j * kT, b);
+        tma_load_4d(sV + c * kT * 128, &tmV, fb, c * 64, kvh, j * kT, b);
+      }
+      int t = 0;
+      bool ok = true;
+      for (; t < nsteps && ok; ++t) {
+        const int st = t & 1, use = t >> 1;
+        if (use > 0 && !wait_bounded(smem_addr(&sy.empty[st]), (use - 1) & 1, sy, p)) {
+          ok = false;
+          break;
+        }
+        const int h = kvh * p.g + t / (p.T - i0);
+        const int i = i0 + t % (p.T - i0);
+        const uint32_t dst = sStage + st * kStage, bar = smem_addr(&sy.full[st]);
+        mbar_arrive_expect_tx(bar, 2 * kTileBytes + 1024);
+        for (int c = 0; c < 2; ++c) {
+          tma_load_4d(dst + c * kT * 128, &tmQ, bar, c * 64, h, i * kT, b);
+          tma_load_4d(dst + kTileBytes + c * kT * 128, &tmdO, bar, c * 64, h, i * kT, b);
+        }
+        const size_t row0 = (static_cast<size_t>(b) * p.n_q + h) * (p.T * kT) + i * kT;
+        bulk_load(dst + 2 * kTileBytes, p.lse2 + row0, 512, bar);
+        bulk_load(dst + 2 * kTileBytes + 512, p.rowdot + row0, 512, bar);
+      }
+      // let every copy land before the CTA can exit
+      wait_drain(smem_addr(&sy.fixed_full), 0);
+      for (int s = 0; s < 2 && s < t; ++s) {
+        const int last = s + ((t - 1 - s) / 2) * 2;
+        wait_drain(smem_addr(&sy.full[s]), (last >> 1) & 1);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    const bool leader = elect_one();
+    bool ok = __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.fixed_full), 0, sy, p));
+    tc_fence_after_sync();
+    for (int t = 0; t < nsteps && ok; ++t) {
+      const int st = t & 1;
+      const uint32_t sQ = sStage + st * kStage, sdO = sQ + kTileBytes;
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.full[st]), (t >> 1) & 1, sy, p))) break;
+      tc_fence_after_sync();
+      mma_rows_x_rows(leader, tmem + 0, sK, sQ);       // S^T  = K Q^T
+      mma_rows_x_rows(leader, tmem + 128, sV, sdO);    // dP^T = V dO^T
+      if (leader) mma_commit(smem_addr(&sy.s_full));
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.p_full), t & 1, sy, p))) break;
+      tc_fence_after_sync();
+      mma_tmem_x_rows(leader, tmem + 256, tmem + 0, sdO, t > 0);    // dV += P^T dO
+      mma_tmem_x_rows(leader, tmem + 384, tmem + 128, sQ, t > 0);   // dK += dS^T Q
+      if (leader) mma_commit(smem_addr(&sy.empty[st]));
+    }
+    if (leader) mma_commit(smem_addr(&sy.done));
+    teardown(sy, p, leader);
+    return;
+  } else {
+    // compute warpgroup: thread r = key row r of the tile = TMEM lane r
+    const int r = warp * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    bool ok = true;
+    for (int t = 0; t < nsteps; ++t) {
+      const int st = t & 1;
+      const int i = i0 + t % (p.T - i0);
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.s_full), t & 1, sy, p))) {
+        ok = false;
+        break;
+      }
+      // the staged row statistics arrived with the stage's copies
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.full[st]), (t >> 1) & 1, sy, p))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const float* lse2 = reinterpret_cast<const float*>(dyn_smem + (sStage + st * kStage + 2 * kTileBytes - smem_addr(dyn_smem)));
+      const float* dd = lse2 + 128;
+      const bool diag = p.causal && i == j;           // query c < key r is masked
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sv[32], dpv[32];
+        tmem_ld32(lane_base + 32 * c, sv);
+        tmem_ld32(lane_base + 128 + 32 * c, dpv);
+        tmem_wait_ld(sv);
+        tmem_after_wait(dpv);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float pp[2], ds[2];
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int col = 32 * c + 2 * e + h2;
+            float pv = ex2_approx(fmaf(__uint_as_float(sv[2 * e + h2]), p.c, -lse2[col]));
+            if (diag && col < r) pv = 0.0f;
+            pp[h2] = pv;
+            ds[h2] = pv * (__uint_as_float(dpv[2 * e + h2]) - dd[col]);
+          }
+          pk[e] = pack_bf16x2(pp[0], pp[1]);
+          dk[e] = pack_bf16x2(ds[0], ds[1]);
+        }
+        tmem_st16(lane_base + 16 * c, pk);            // P^T over the consumed S^T columns
+        tmem_st16(lane_base + 128 + 16 * c, dk);      // dS^T over the consumed dP^T columns
+      }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(smem_addr(&sy.p_full));
+    }
+    if (ok && __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.done), 0, sy, p))) {
+      tc_fence_after_sync();
+      const int row = j * kT + r;
+      const bool valid = row < p.L;
+      const size_t off = ((static_cast<size_t>(b) * p.L + row) * p.n_kv + kvh) * kD;
+      store_row(lane_base + 256, p.dv + off, 1.0f, valid);
+      store_row(lane_base + 384, p.dk + off, p.scale, valid);
+    }
+  }
+  teardown(sy, p, false);
+}
+
+// ------------------------------------------------------------------------ dQ
+
+__global__ void __launch_bounds__(kThreads, 1)
+dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+          const BwdParams p) {
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ Sync sy;
+  // smem: Q_i | dO_i | stage 0: K_j, V_j | stage 1: K_j, V_j
+  const uint32_t base = (smem_addr(dyn_smem) + 1023u) & ~1023u;
+  const uint32_t sQ = base, sdO = base + kTileBytes;
+  constexpr uint32_t kStage = 2 * kTileBytes;
+  const uint32_t sStage = base + 2 * kTileBytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int groups = static_cast<int>(gridDim.x) / p.T;   // B * n_q
+  const int i = p.T - 1 - static_cast<int>(blockIdx.x) / groups;   // longest first
+  const int grp = blockIdx.x - (p.T - 1 - i) * groups;
+  const int b = grp / p.n_q, h = grp - b * p.n_q;
+  const int kvh = h / p.g;
+  const int n = p.causal ? i + 1 : p.T;
+  setup(sy, 128);
+  const uint32_t tmem = sy.tmem_base;
+
+  if (warp == kLoadWarp) {
+    if (lane == 0) {
+      const uint32_t fb = smem_addr(&sy.fixed_full);
+      mbar_arrive_expect_tx(fb, 2 * kTileBytes);
+      for (int c = 0; c < 2; ++c) {
+        tma_load_4d(sQ + c * kT * 128, &tmQ, fb, c * 64, h, i * kT, b);
+        tma_load_4d(sdO + c * kT * 128, &tmdO, fb, c * 64, h, i * kT, b);
+      }
+      int t = 0;
+      for (; t < n; ++t) {
+        const int st = t & 1, use = t >> 1;
+        if (use > 0 && !wait_bounded(smem_addr(&sy.empty[st]), (use - 1) & 1, sy, p)) break;
+        const uint32_t dst = sStage + st * kStage, bar = smem_addr(&sy.full[st]);
+        mbar_arrive_expect_tx(bar, 2 * kTileBytes);
+        for (int c = 0; c < 2; ++c) {
+          tma_load_4d(dst + c * kT * 128, &tmK, bar, c * 64, kvh, t * kT, b);
+          tma_load_4d(dst + kTileBytes + c * kT * 128, &tmV, bar, c * 64, kvh, t * kT, b);
+        }
+      }
+      wait_drain(smem_addr(&sy.fixed_full), 0);
+      for (int s = 0; s < 2 && s < t; ++s) {
+        const int last = s + ((t - 1 - s) / 2) * 2;
+        wait_drain(smem_addr(&sy.full[s]), (last >> 1) & 1);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    const bool leader = elect_one();
+    bool ok = __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.fixed_full), 0, sy, p));
+    tc_fence_after_sync();
+    for (int t = 0; t < n && ok; ++t) {
+      const int st = t & 1;
+      const uint32_t sK = sStage + st * kStage, sV = sK + kTileBytes;
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.full[st]), (t >> 1) & 1, sy, p))) break;
+      tc_fence_after_sync();
+      mma_rows_x_rows(leader, tmem + 0, sQ, sK);       // S  = Q K^T
+      mma_rows_x_rows(leader, tmem + 128, sdO, sV);    // dP = dO V^T
+      if (leader) mma_commit(smem_addr(&sy.s_full));
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.p_full), t & 1, sy, p))) break;
+      tc_fence_after_sync();
+      mma_tmem_x_rows(leader, tmem + 256, tmem + 0, sK, t > 0);     // dQ += dS K
+      if (leader) mma_commit(smem_addr(&sy.empty[st]));
+    }
+    if (leader) mma_commit(smem_addr(&sy.done));
+    teardown(sy, p, leader);
+    return;
+  } else {
+    // compute warpgroup: thread r = query row r of the tile = TMEM lane r
+    const int r = warp * 32 + lane;
+    const int row = i * kT + r;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const size_t srow = (static_cast<size_t>(b) * p.n_q + h) * (p.T * kT) + row;
+    const float lse2 = p.lse2[srow], dd = p.rowdot[srow];
+    bool ok = true;
+    for (int t = 0; t < n; ++t) {
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.s_full), t & 1, sy, p))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      // keys after `keep` (in-tile) are masked: the diagonal tile, or keys past L
+      const bool masked = p.causal ? (t == i) : (p.L - t * kT < kT);
+      const int keep = p.causal ? r : p.L - 1 - t * kT;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sv[32], dpv[32];
+        tmem_ld32(lane_base + 32 * c, sv);
+        tmem_ld32(lane_base + 128 + 32 * c, dpv);
+        tmem_wait_ld(sv);
+        tmem_after_wait(dpv);
+        uint32_t dk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float ds[2];
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int col = 32 * c + 2 * e + h2;
+            float pv = ex2_approx(fmaf(__uint_as_float(sv[2 * e + h2]), p.c, -lse2));
+            if (masked && col > keep) pv = 0.0f;
+            ds[h2] = pv * (__uint_as_float(dpv[2 * e + h2]) - dd);
+          }
+          dk[e] = pack_bf16x2(ds[0], ds[1]);
+        }
+        tmem_st16(lane_base + 16 * c, dk);            // dS over the consumed S columns
+      }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(smem_addr(&sy.p_full));
+    }
+    if (ok && __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.done), 0, sy, p))) {
+      tc_fence_after_sync();
+      const size_t off = ((static_cast<size_t>(b) * p.L + row) * p.n_q + h) * kD;
+      store_row(lane_base + 256, p.dq + off, p.scale, row < p.L);
+    }
+  }
+  teardown(sy, p, false);
+}
+
+// --------------------------------------------------------------------- host
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+constexpr int kMaxDevices = 64;
+std::mutex g_bwd_mutex;
+bool g_bwd_ready[kMaxDevices];
+EncodeTiledFn g_bwd_encode = nullptr;
+constexpr int kDkdvSmem = 2 * kTileBytes + 2 * (2 * kTileBytes + 1024) + 1024;
+constexpr int kDqSmem = 2 * kTileBytes + 2 * (2 * kTileBytes) + 1024;
+
+attn_status_t bwd_device_ready(cudaStream_t stream, int** status) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  // device check, tensor-map encoder and status word come from the forward's set-up
+  const attn_status_t ds = gb300_host::device_status_word(stream, status);
+  if (ds != ATTN_OK) return ds;
+  std::lock_guard<std::mutex> lock(g_bwd_mutex);
+  if (!g_bwd_ready[dev]) {
+    if (!g_bwd_encode) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return ATTN_ERR_CUDA;
+      g_bwd_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    if (cudaFuncSetAttribute(dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kDkdvSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDqSmem) !=
+            cudaSuccess)
+      return ATTN_ERR_CUDA;
+    g_bwd_ready[dev] = true;
+  }
+  return ATTN_OK;
+}
+
+bool encode_tile_map(CUtensorMap* map, const void* ptr, int H, int64_t L, int64_t B) {
+  const cuuint64_t dims[4] = {kD, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(L),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {kD * 2, static_cast<cuuint64_t>(H) * kD * 2,
+                                 static_cast<cuuint64_t>(L) * H * kD * 2};
+  const cuuint32_t box[4] = {64, 1, kT, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  return g_bwd_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims,
+                      strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t attn_prefill_bwd_workspace_bytes(int64_t B, int64_t L, int32_t n_q, int32_t n_kv,
+                                         int32_t d_h) {
+  if (B < 1 || L < 1 || n_q < 1 || n_kv < 1 || n_q % n_kv != 0 || d_h != kD) return -1;
+  const int64_t T = (L + kT - 1) / kT;
+  return 2 * B * n_q * T * kT * 4;
+}
+
+attn_status_t attn_prefill_bwd(const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                               void* workspace, int64_t workspace_bytes, int64_t B, int64_t L,
+                               int32_t n_q, int32_t n_kv, int32_t d_h, int32_t causal,
+                               float scale, void* stream_ptr) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace)
+    return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || L < 1 || n_q < 1 || n_kv < 1 || n_q % n_kv != 0) return ATTN_ERR_INVALID_ARG;
+  if ((causal != 0 && causal != 1) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  auto misaligned = [](const void* ptr, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0;
+  };
+  if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(o, 16) ||
+      misaligned(dout, 16) || misaligned(dq, 16) || misaligned(dk, 16) || misaligned(dv, 16) ||
+      misaligned(lse, 4) || misaligned(workspace, 16))
+    return ATTN_ERR_INVALID_ARG;
+  if (d_h != kD) return ATTN_ERR_UNSUPPORTED;
+  const int64_t T = (L + kT - 1) / kT;
+  if (L > (int64_t{1} << 30) || B * n_kv * T > INT32_MAX || B * n_q * T > INT32_MAX)
+    return ATTN_ERR_UNSUPPORTED;
+  if (workspace_bytes < attn_prefill_bwd_workspace_bytes(B, L, n_q, n_kv, d_h))
+    return ATTN_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  int* status = nullptr;
+  const attn_status_t ds = bwd_device_ready(stream, &status);
+  if (ds != ATTN_OK) return ds;
+
+  CUtensorMap mq, mk, mv, mdo;
+  if (!encode_tile_map(&mq, q, n_q, L, B) || !encode_tile_map(&mk, k, n_kv, L, B) ||
+      !encode_tile_map(&mv, v, n_kv, L, B) || !encode_tile_map(&mdo, dout, n_q, L, B))
+    return ATTN_ERR_CUDA;
+  BwdParams p;
+  p.L = static_cast<int>(L);
+  p.n_q = n_q;
+  p.n_kv = n_kv;
+  p.g = n_q / n_kv;
+  p.T = static_cast<int>(T);
+  p.causal = causal;
+  p.c = scale * kLog2e;
+  p.scale = scale;
+  float* lse2 = static_cast<float*>(workspace);
+  float* rowdot = lse2 + B * n_q * T * kT;
+  p.lse2 = lse2;
+  p.rowdot = rowdot;
+  p.dq = static_cast<uint16_t*>(dq);
+  p.dk = static_cast<uint16_t*>(dk);
+  p.dv = static_cast<uint16_t*>(dv);
+  p.status = status;
+
+  const int64_t rows = B * n_q * T * kT;
+  rowdot_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, lse2, rowdot,
+      static_cast<int>(B), static_cast<int>(L), n_q, static_cast<int>(T * kT));
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  dkdv_kernel<<<static_cast<unsigned>(B * n_kv * T), kThreads, kDkdvSmem, stream>>>(mq, mk, mv,
+                                                                                     mdo, p);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  dq_kernel<<<static_cast<unsigned>(B * n_q * T), kThreads, kDqSmem, stream>>>(mq, mk, mv, mdo, p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // extern "C"

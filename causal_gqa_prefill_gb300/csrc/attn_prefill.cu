@@ -782,6 +782,18 @@ attn_status_t launch_forward(const void* q, const void* k, const void* v, void* 
 
 }  // namespace
 
+// The per-device status word (allocated on first use) for the other kernels of
+// this library, so that attn_device_check reports their timeouts as well.
+namespace gb300_host {
+attn_status_t device_status_word(cudaStream_t stream, int** status) {
+  DeviceState* st = nullptr;
+  const attn_status_t ds = device_state(stream, &st);
+  if (ds != ATTN_OK) return ds;
+  *status = st->status;
+  return ATTN_OK;
+}
+}  // namespace gb300_host
+
 extern "C" {
 
 attn_status_t attn_prefill_fwd_chunk(const void* q, const void* k, const void* v, void* o,

@@ -8,7 +8,9 @@ Recipe: seed = 1000 + config number; a torch.Generator on the target device
 draws Q, K, V in that order as float32 N(0, 1), each rounded to bf16 (round to
 nearest even). The 70B-shaped workload multiplies K channels 0..3 of every
 K/V head by 8 (N(0, 8^2) there), which pushes single logits far above the
-rest and exercises the online-softmax rescaling.
+rest and exercises the online-softmax rescaling. Backward workloads draw
+the upstream gradient dO after Q, K, V from a second generator seeded with
+seed + 500000, float32 N(0, 1) rounded to bf16.
 """
 
 from __future__ import annotations
@@ -31,6 +33,7 @@ class Workload:
     Lk: int = 0                     # keys (0: = L); L < Lk makes Q the last L positions
     dtype: str = "bf16"             # "bf16" or "e4m3" (Q, K, V stored as fp8, descale 1)
     decode: bool = False            # one query token per sequence against Lk cached keys
+    backward: bool = False          # gradients (dQ, dK, dV) for a seeded upstream dO
 
     @property
     def keys(self) -> int:
@@ -60,12 +63,20 @@ class Workload:
         2*n_q*d_h*(2*L*offset + L^2)*B (equal to the square count at offset 0).
         """
         if self.decode or not self.causal:
-            return 4 * self.n_q * self.d_h * self.L * self.keys * self.B
-        return 2 * self.n_q * self.d_h * (2 * self.L * self.offset + self.L * self.L) * self.B
+            f = 4 * self.n_q * self.d_h * self.L * self.keys * self.B
+        else:
+            f = 2 * self.n_q * self.d_h * (2 * self.L * self.offset + self.L * self.L) * self.B
+        # backward: five products of the forward's size (S, dP, dV, dK, dQ) against
+        # the forward's two, i.e. 2.5x the forward count
+        return f * 5 // 2 if self.backward else f
 
     def io_bytes(self) -> int:
-        """Bytes read and written once: Q, K, V, O in bf16 and LSE in fp32."""
+        """Bytes read and written once: Q, K, V, O in bf16 and LSE in fp32 (the
+        backward adds dO read and dQ, dK, dV written)."""
         e = self.B * self.d_h * 2
+        if self.backward:
+            return (e * (4 * self.n_q * self.L + 4 * self.n_kv * self.keys)
+                    + self.B * self.n_q * self.L * 4)
         return (e * (2 * self.n_q * self.L + 2 * self.n_kv * self.keys)
                 + self.B * self.n_q * self.L * 4)
 
@@ -78,6 +89,8 @@ class Workload:
             d["inputs"] = self.dtype
         if self.decode:
             d["step"] = "decode"
+        if self.backward:
+            d["step"] = "backward"
         return d
 
 
@@ -110,6 +123,9 @@ WORKLOADS = {
                  decode=True),
     11: Workload(11, "decode, 36-head shape after a 131072-token prompt (B=1, Lk=131072, n_q=36, "
                      "n_kv=6, d_h=128)", 1, 1, 36, 6, 128, Lk=131072, decode=True),
+    # backward: gradients of the Llama-3-8B-shaped layer
+    12: Workload(12, "backward, Llama-3-8B-shaped layer, GQA-4 (B=1, L=8192, n_q=32, n_kv=8, "
+                     "d_h=128)", 1, 8192, 32, 8, 128, full_check=False, backward=True),
 }
 
 
@@ -131,10 +147,20 @@ def make_inputs(w: Workload, device="cuda", seed: int | None = None):
     return q, k, v
 
 
+def make_grad(w: Workload, device="cuda", seed: int | None = None):
+    """Seeded bf16 upstream gradient dO [B, L, n_q, d_h] for a backward workload."""
+    import torch
+
+    gen = torch.Generator(device=device)
+    gen.manual_seed((w.seed if seed is None else seed) + 500000)
+    shape = (w.B, w.L, w.n_q, w.d_h)
+    return torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
 def custom(B, L, n_q, n_kv, d_h, causal=True, number=0, name=None, Lk=0,
-           dtype="bf16") -> Workload:
+           dtype="bf16", backward=False) -> Workload:
     return Workload(number, name or f"B={B} L={L} Lk={Lk or L} n_q={n_q} n_kv={n_kv} d_h={d_h}",
-                    B, L, n_q, n_kv, d_h, causal, Lk=Lk, dtype=dtype)
+                    B, L, n_q, n_kv, d_h, causal, Lk=Lk, dtype=dtype, backward=backward)
 
 
 def sampled_rows(w: Workload, count: int = 4096, tile: int = 128):

@@ -149,6 +149,40 @@ attn_status_t attn_decode_fwd(const void* q, const void* k, const void* v, void*
                               int64_t B, int64_t Lk, int32_t n_q, int32_t n_kv, int32_t d_h,
                               float scale, void* stream);
 
+/*
+ * Backward pass: gradients of attn_prefill_fwd with respect to q, k and v for
+ * an upstream gradient dout, computed by rebuilding the score tiles from q, k
+ * and the forward's lse instead of storing the L x L table ("Long-Context
+ * Attention Explained" (sevydevy), "What FlashAttention does not change":
+ * the backward pass recomputes the blocks from the saved row statistics).
+ * With P the forward's softmax weights (masked entries 0), D_i = dout_i . o_i:
+ *
+ *     dV_j = sum_i P_ij dout_i                 dP_ij = dout_i . V_j
+ *     dS_ij = P_ij (dP_ij - D_i)
+ *     dQ_i = scale sum_j dS_ij K_j             dK_j = scale sum_i dS_ij Q_i
+ *
+ * where the sums for dK and dV run over every query head of the K/V head's
+ * group. No atomics: results are deterministic.
+ *
+ *   q, k, v, o, lse   the forward's inputs and outputs (layouts above)
+ *   dout              bf16 [B, L, n_q, d_h], 16-byte aligned
+ *   dq                bf16 [B, L, n_q, d_h]   written
+ *   dk, dv            bf16 [B, L, n_kv, d_h]  written
+ *   workspace         device memory of at least attn_prefill_bwd_workspace_bytes
+ *                     bytes, 16-byte aligned, owned by the caller; contents on
+ *                     entry ignored, on exit unspecified
+ *   d_h must be 128 (ATTN_ERR_UNSUPPORTED otherwise); square problems only
+ *   (the forward's Lq = Lk = L). Everything else as attn_prefill_fwd.
+ */
+int64_t attn_prefill_bwd_workspace_bytes(int64_t B, int64_t L, int32_t n_q, int32_t n_kv,
+                                         int32_t d_h);   /* -1 on invalid or unsupported sizes */
+attn_status_t attn_prefill_bwd(const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, const void* dout,
+                               void* dq, void* dk, void* dv,
+                               void* workspace, int64_t workspace_bytes,
+                               int64_t B, int64_t L, int32_t n_q, int32_t n_kv, int32_t d_h,
+                               int32_t causal, float scale, void* stream);
+
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* attn_status_string(attn_status_t status);
 

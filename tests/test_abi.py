@@ -124,6 +124,30 @@ def test_decode_workspace_and_validation(lib):
     assert cg.attn_decode_fwd(*bad, stream=0) == cg.ATTN_ERR_UNSUPPORTED
 
 
+def test_backward_workspace_and_validation(lib):
+    need = cg.attn_prefill_bwd_workspace_bytes(2, 300, 8, 2)
+    assert need == 2 * 2 * 8 * 384 * 4        # LSE*log2(e) and D, padded to 128-row tiles
+    assert cg.attn_prefill_bwd_workspace_bytes(2, 300, 8, 2, 64) == -1
+    assert cg.attn_prefill_bwd_workspace_bytes(2, 300, 8, 3) == -1
+    assert cg.attn_prefill_bwd_workspace_bytes(0, 300, 8, 2) == -1
+    args = [FAKE] * 10 + [need, 2, 300, 8, 2, 128, 1, 0.1]
+    for idx in range(10):                                # every pointer is required
+        bad = list(args); bad[idx] = 0
+        assert cg.attn_prefill_bwd(*bad, stream=0) == cg.ATTN_ERR_INVALID_ARG, idx
+    bad = list(args); bad[5] = FAKE + 2                  # dout misaligned
+    assert cg.attn_prefill_bwd(*bad, stream=0) == cg.ATTN_ERR_INVALID_ARG
+    bad = list(args); bad[10] = need - 16                # workspace too small
+    assert cg.attn_prefill_bwd(*bad, stream=0) == cg.ATTN_ERR_INVALID_ARG
+    bad = list(args); bad[16] = 2                        # causal not 0/1
+    assert cg.attn_prefill_bwd(*bad, stream=0) == cg.ATTN_ERR_INVALID_ARG
+    bad = list(args); bad[17] = math.inf
+    assert cg.attn_prefill_bwd(*bad, stream=0) == cg.ATTN_ERR_INVALID_ARG
+    bad = list(args); bad[14] = 3                        # n_q % n_kv
+    assert cg.attn_prefill_bwd(*bad, stream=0) == cg.ATTN_ERR_INVALID_ARG
+    bad = list(args); bad[15] = 64                       # head dim
+    assert cg.attn_prefill_bwd(*bad, stream=0) == cg.ATTN_ERR_UNSUPPORTED
+
+
 def test_chunk_workload_flops_reduce_to_square():
     w = workloads.custom(1, 300, 4, 2, 64, Lk=300)
     assert w.metric_flops() == oflops.causal_attention_flops(1, 300, 4, 64)
@@ -148,7 +172,9 @@ def test_wrapper_rejects_host_tensors():
 def test_metric_flops_match_the_oracle_cost_model():
     for w in workloads.WORKLOADS.values():
         if w.keys == w.L:
-            assert w.metric_flops() == oflops.causal_attention_flops(w.B, w.L, w.n_q, w.d_h)
+            fwd = oflops.causal_attention_flops(w.B, w.L, w.n_q, w.d_h)
+            # backward: five products of the forward's size against its two
+            assert w.metric_flops() == (fwd * 5 // 2 if w.backward else fwd)
 
 
 def test_sampled_rows_cover_heads_and_tile_positions():

@@ -1,0 +1,163 @@
+"""GPU parity of the backward pass (dQ, dK, dV) against the fp64 oracle.
+
+The CUDA path: the product's forward (O, LSE) followed by attn_prefill_bwd,
+both through the C ABI. The oracle: oracle.attention_backward on the same
+bf16 inputs in float64. Large workloads are checked on whole K/V head groups
+(the g query heads that share one K/V head and that K/V head), which are
+independent of the other groups, so the oracle's output for a group is exact
+for that slice.
+
+Acceptance per gradient G (dQ, dK, dV), derived from the arithmetic of the
+kernels: P and dS are rounded to bf16 before the products that consume them
+(relative error <= 2^-9 each), D comes from the bf16 forward output O, the
+products accumulate in fp32, and G is rounded to bf16 at the end
+(<= 2^-9 |G| relative). Summed over the terms of a gradient element, the
+first three give errors of a few 2^-9 of the RMS of G's terms; the bounds are
+  * ||err||_F / ||G_ref||_F <= 1e-2
+  * max |err| <= 2^-6 * max |G_ref| + 2^-8 * |G_ref|   (element-wise)
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from causal_gqa_prefill_gb300 import (ATTN_OK, ATTN_ERR_UNSUPPORTED, AttnError, attn_device_check,
+                                      attn_prefill, attn_prefill_backward)
+from causal_gqa_prefill_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+REL_FRO = 1e-2
+ABS_OF_MAX = 2.0 ** -6
+REL_ELEM = 2.0 ** -8
+
+
+def to_np(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def grad_errors(g_gpu, g_ref):
+    d = g_gpu - g_ref
+    ref_max = float(np.abs(g_ref).max()) if g_ref.size else 0.0
+    fro = float(np.linalg.norm(d) / max(np.linalg.norm(g_ref), 1e-30))
+    excess = np.abs(d) - (ABS_OF_MAX * ref_max + REL_ELEM * np.abs(g_ref))
+    return {"rel_fro": fro, "max_abs": float(np.abs(d).max()) if d.size else 0.0,
+            "ref_max": ref_max, "excess": float(excess.max()) if d.size else 0.0}
+
+
+def assert_grads(gpu, ref, what=""):
+    out = {}
+    for name, g, r in zip(("dq", "dk", "dv"), gpu, ref):
+        e = grad_errors(to_np(g), r)
+        out[name] = e
+        assert np.isfinite(e["max_abs"]), (what, name, e)
+        assert e["rel_fro"] <= REL_FRO, (what, name, e)
+        assert e["excess"] <= 0.0, (what, name, e)
+    return out
+
+
+def run_backward(q, k, v, dout, causal=True, scale=None):
+    o, lse = attn_prefill(q, k, v, causal=causal, scale=scale)
+    dq, dk, dv = attn_prefill_backward(q, k, v, o, lse, dout, causal=causal, scale=scale)
+    assert attn_device_check() == ATTN_OK
+    return dq, dk, dv
+
+
+def inputs(B, L, n_q, n_kv, causal=True, number=0):
+    w = W.custom(B, L, n_q, n_kv, 128, causal=causal, number=number, backward=True)
+    q, k, v = W.make_inputs(w)
+    return w, q, k, v, W.make_grad(w)
+
+
+SHAPES = [
+    # B, L, n_q, n_kv, causal
+    (1, 128, 2, 2, True),        # one tile
+    (1, 300, 4, 2, True),        # ragged tail
+    (2, 640, 8, 2, True),        # batch, GQA-4, several tiles
+    (1, 257, 6, 6, True),        # MHA, one-row tail
+    (1, 333, 4, 1, False),       # full attention, MQA, ragged
+    (1, 1000, 8, 1, True),       # GQA-8 (one K/V head collects 8 query heads)
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[f"B{s[0]}L{s[1]}h{s[2]}-{s[3]}{'c' if s[4] else 'f'}"
+                                               for s in SHAPES])
+def test_backward_small_shapes(shape):
+    B, L, n_q, n_kv, causal = shape
+    w, q, k, v, dout = inputs(B, L, n_q, n_kv, causal, number=1200 + L)
+    gpu = run_backward(q, k, v, dout, causal=causal)
+    ref = oracle.attention_backward(to_np(q), to_np(k), to_np(v), to_np(dout), causal=causal)
+    errs = assert_grads(gpu, ref, str(shape))
+    print(shape, errs)
+
+
+def test_backward_single_row_closed_form():
+    # L = 1: the softmax has one entry (P = 1), so dV = dO summed over the group
+    # and dS = dP - D = dO.V - dO.O = 0, hence dQ = dK = 0. On the GPU dP (tensor
+    # cores) and D (row kernel) are two fp32 sums of the same 128 products in
+    # different orders, so dS is zero up to fp32 rounding of a dot product of
+    # size |dO||V| ~ 128: |dQ|, |dK| <= scale * 128 * 1e-5 * |K|, well under 1e-3.
+    w, q, k, v, dout = inputs(1, 1, 4, 2, True, number=1301)
+    dq, dk, dv = run_backward(q, k, v, dout)
+    assert dq.float().abs().max().item() <= 1e-3
+    assert dk.float().abs().max().item() <= 1e-3
+    want = dout.float().view(1, 1, 2, 2, 128).sum(3)
+    assert torch.allclose(dv.float(), want, rtol=2 ** -8, atol=0)
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.05, 0.25])
+def test_backward_scales(scale):
+    w, q, k, v, dout = inputs(1, 384, 4, 2, True, number=1302)
+    gpu = run_backward(q, k, v, dout, scale=scale)
+    ref = oracle.attention_backward(to_np(q), to_np(k), to_np(v), to_np(dout), causal=True,
+                                    scale=scale)
+    if scale == 0.0:
+        # uniform weights: dQ = dK = 0 exactly (scale multiplies both)
+        assert torch.count_nonzero(gpu[0]).item() == 0
+        assert torch.count_nonzero(gpu[1]).item() == 0
+        assert grad_errors(to_np(gpu[2]), ref[2])["rel_fro"] <= REL_FRO
+    else:
+        assert_grads(gpu, ref, f"scale={scale}")
+
+
+def test_backward_deterministic():
+    w, q, k, v, dout = inputs(1, 700, 8, 2, True, number=1303)
+    a = run_backward(q, k, v, dout)
+    b = run_backward(q, k, v, dout)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_backward_head_dim_64_unsupported():
+    w = W.custom(1, 128, 2, 1, 64)
+    q, k, v = W.make_inputs(w)
+    o, lse = attn_prefill(q, k, v)
+    with pytest.raises(AttnError) as e:
+        attn_prefill_backward(q, k, v, o, lse, torch.randn_like(q))
+    assert e.value.status == ATTN_ERR_UNSUPPORTED
+
+
+def _group_slice(w, q, k, v, dout, kvh):
+    hs = slice(kvh * w.g, (kvh + 1) * w.g)
+    return (to_np(q[:, :, hs]), to_np(k[:, :, kvh:kvh + 1]), to_np(v[:, :, kvh:kvh + 1]),
+            to_np(dout[:, :, hs]))
+
+
+@pytest.mark.parametrize("num,groups", [(2, [(0, 0), (3, 31)]), (12, [(0, 0), (0, 7)])])
+def test_backward_workload_groups(num, groups):
+    """Model-shaped layers at full size; the oracle checks whole head groups
+    ((batch, K/V head) pairs listed per workload)."""
+    base = W.WORKLOADS[num]
+    w = W.custom(base.B, base.L, base.n_q, base.n_kv, base.d_h, number=base.number,
+                 backward=True)
+    q, k, v = W.make_inputs(w)
+    dout = W.make_grad(w)
+    dq, dk, dv = run_backward(q, k, v, dout)
+    for b, kvh in groups:
+        hs = slice(kvh * w.g, (kvh + 1) * w.g)
+        qs, ks, vs, ds = _group_slice(w, q[b:b + 1], k[b:b + 1], v[b:b + 1], dout[b:b + 1], kvh)
+        ref = oracle.attention_backward(qs, ks, vs, ds, causal=True)
+        gpu = (dq[b:b + 1, :, hs], dk[b:b + 1, :, kvh:kvh + 1], dv[b:b + 1, :, kvh:kvh + 1])
+        errs = assert_grads(gpu, ref, f"workload {num} group ({b}, {kvh})")
+        print(num, b, kvh, errs)
