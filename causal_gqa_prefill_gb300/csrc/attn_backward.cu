@@ -22,7 +22,12 @@
 //   dq      one CTA per (b, query head, 128-row tile i): S = Q K^T and
 //           dP = dO V^T, dS in TMEM, dQ += dS K over the key tiles it sees.
 // Each kernel has a TMA producer warp, an MMA warp (warp-wide loop, one elected
-// issuing lane) and a 128-thread compute warpgroup (thread = TMEM lane).
+// issuing lane) and kComputeWGs compute warpgroups that split the columns of
+// each score tile (thread = TMEM lane = tile row; warpgroup w owns columns
+// [w*C, w*C + C), C = 128 / kComputeWGs). A warpgroup writes its bf16 P/dS
+// back over the first C/2 of its own, already consumed, fp32 columns, so no
+// warpgroup ever overwrites columns another one still has to read; the
+// products that consume P/dS take their A operand K-step by K-step from there.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -44,8 +49,13 @@ using namespace gb300;
 constexpr int kD = 128;                  // head dimension
 constexpr int kT = 128;                  // rows per query tile and keys per key tile
 constexpr int kTileBytes = kT * kD * 2;  // one bf16 128 x 128 tile (two 64-column chunks)
-constexpr int kThreads = 192;            // warps 0-3 compute, 4 producer, 5 MMA
-constexpr int kLoadWarp = 4, kMmaWarp = 5;
+constexpr int kComputeWGs = 2;                       // compute warpgroups
+constexpr int kCols = kT / kComputeWGs;                // tile columns per warpgroup
+constexpr int kComputeThreads = 128 * kComputeWGs;
+constexpr int kLoadWarp = 4 * kComputeWGs, kMmaWarp = kLoadWarp + 1;
+// producer and MMA warps plus two idle warps: registers are granted per
+// four warps, so the CTA is a whole number of warpgroups
+constexpr int kThreads = kComputeThreads + 128;
 constexpr long long kSpinLimit = 1ll << 31;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -54,8 +64,8 @@ struct BwdParams {
   int causal;
   float c;                  // scale * log2(e)
   float scale;
-  const float* lse2;        // [B, n_q, T*128] LSE * log2(e), +inf past L
-  const float* rowdot;      // [B, n_q, T*128] D, 0 past L
+  const float* nlse2;       // [B, n_q, T*128] -LSE * log2(e), -inf past L
+  const float* nrowdot;     // [B, n_q, T*128] -D, 0 past L
   uint16_t* dq;             // bf16 [B, L, n_q, 128]
   uint16_t* dk;             // bf16 [B, L, n_kv, 128]
   uint16_t* dv;
@@ -110,6 +120,19 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// TMEM column (relative to the score tile's base) holding the bf16 A operand
+// for K step kk (tile columns 16*kk .. 16*kk + 15): warpgroup w packs its
+// columns [w*C, w*C + C) two per 32-bit column starting at column w*C.
+__host__ __device__ constexpr uint32_t a_col(int kk) {
+  return static_cast<uint32_t>((16 * kk / kCols) * kCols + (16 * kk % kCols) / 2);
+}
+
 // 128x128x128 product into TMEM, A and B [128 rows x 128] K-major bf16 tiles.
 __device__ __forceinline__ void mma_rows_x_rows(bool leader, uint32_t d_tmem, uint32_t a_smem,
                                                 uint32_t b_smem) {
@@ -131,7 +154,7 @@ __device__ __forceinline__ void mma_tmem_x_rows(bool leader, uint32_t d_tmem, ui
 #pragma unroll
   for (int kk = 0; kk < kT / 16; ++kk) {
     const uint64_t b = sdesc_sw128(b_smem + kk * 16 * 128, kT * 128, 1024);
-    if (leader) mma_ts(d_tmem, a_tmem + kk * 8, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
+    if (leader) mma_ts(d_tmem, a_tmem + a_col(kk), b, idesc, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -172,29 +195,26 @@ __device__ __forceinline__ void teardown(Sync& sy, const BwdParams& p, bool lead
   }
 }
 
-// bf16 output row (128 values) from 4 x 32 fp32 TMEM columns, times `mul`.
-__device__ __forceinline__ void store_row(uint32_t t_row, uint16_t* dst, float mul, bool valid) {
-#pragma unroll 1
-  for (int c = 0; c < kD; c += 32) {
-    uint32_t v[32];
-    tmem_ld32(t_row + c, v);
-    tmem_wait_ld(v);
-    uint32_t w[16];
+// 32 bf16 outputs of this thread's row from 32 fp32 TMEM columns, times `mul`.
+__device__ __forceinline__ void store_chunk(uint32_t taddr, uint16_t* dst, float mul, bool valid) {
+  uint32_t v[32];
+  tmem_ld32(taddr, v);
+  tmem_wait_ld(v);
+  uint32_t w[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      w[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
-    if (valid) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+  for (int i = 0; i < 16; ++i)
+    w[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+  if (valid) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-    }
+    for (int q = 0; q < 4; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
   }
 }
 
 // ------------------------------------------------------------------ rowdot
 
 __global__ void rowdot_kernel(const uint16_t* o, const uint16_t* dout, const float* lse,
-                              float* lse2, float* rowdot, int B, int L, int n_q, int Lp) {
+                              float* nlse2, float* nrowdot, int B, int L, int n_q, int Lp) {
   // one warp per padded row (b, h, t); t < Lp
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -217,8 +237,8 @@ __global__ void rowdot_kernel(const uint16_t* o, const uint16_t* dout, const flo
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, off);
   if (lane == 0) {
-    rowdot[row] = dd;
-    lse2[row] = (t < L) ? lse[bh * L + t] * kLog2e : INFINITY;
+    nrowdot[row] = -dd;
+    nlse2[row] = (t < L) ? -lse[bh * L + t] * kLog2e : -INFINITY;
   }
 }
 
@@ -242,7 +262,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   const int b = grp / p.n_kv, kvh = grp - b * p.n_kv;
   const int i0 = p.causal ? j : 0;
   const int nsteps = p.g * (p.T - i0);                 // (head, query tile) pairs
-  setup(sy, 128);
+  setup(sy, kComputeThreads);
   const uint32_t tmem = sy.tmem_base;
 
   if (warp == kLoadWarp) {
@@ -270,8 +290,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           tma_load_4d(dst + kTileBytes + c * kT * 128, &tmdO, bar, c * 64, h, i * kT, b);
         }
         const size_t row0 = (static_cast<size_t>(b) * p.n_q + h) * (p.T * kT) + i * kT;
-        bulk_load(dst + 2 * kTileBytes, p.lse2 + row0, 512, bar);
-        bulk_load(dst + 2 * kTileBytes + 512, p.rowdot + row0, 512, bar);
+        bulk_load(dst + 2 * kTileBytes, p.nlse2 + row0, 512, bar);
+        bulk_load(dst + 2 * kTileBytes + 512, p.nrowdot + row0, 512, bar);
       }
       // let every copy land before the CTA can exit
       wait_drain(smem_addr(&sy.fixed_full), 0);
@@ -301,10 +321,13 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     if (leader) mma_commit(smem_addr(&sy.done));
     teardown(sy, p, leader);
     return;
-  } else {
-    // compute warpgroup: thread r = key row r of the tile = TMEM lane r
-    const int r = warp * 32 + lane;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  } else if (warp < 4 * kComputeWGs) {
+    // compute warpgroups: thread r = key row r of the tile = TMEM lane r;
+    // warpgroup cw takes query columns [cw*kCols, cw*kCols + kCols)
+    const int cw = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint64_t c2 = f32x2_pack(p.c, p.c);
     bool ok = true;
     for (int t = 0; t < nsteps; ++t) {
       const int st = t & 1;
@@ -319,33 +342,47 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         break;
       }
       tc_fence_after_sync();
-      const float* lse2 = reinterpret_cast<const float*>(dyn_smem + (sStage + st * kStage + 2 * kTileBytes - smem_addr(dyn_smem)));
-      const float* dd = lse2 + 128;
+      const float4* nl4 = reinterpret_cast<const float4*>(
+          dyn_smem + (sStage + st * kStage + 2 * kTileBytes - smem_addr(dyn_smem)));
+      const float4* nd4 = nl4 + 32;
       const bool diag = p.causal && i == j;           // query c < key r is masked
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < kCols / 32; ++c) {
+        const int col0 = cw * kCols + 32 * c;
         uint32_t sv[32], dpv[32];
-        tmem_ld32(lane_base + 32 * c, sv);
-        tmem_ld32(lane_base + 128 + 32 * c, dpv);
+        tmem_ld32(lane_base + col0, sv);
+        tmem_ld32(lane_base + 128 + col0, dpv);
         tmem_wait_ld(sv);
         tmem_after_wait(dpv);
         uint32_t pk[16], dk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float pp[2], ds[2];
+        for (int e = 0; e < 8; ++e) {
+          const float4 nl = nl4[col0 / 4 + e], nd = nd4[col0 / 4 + e];
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
-            const int col = 32 * c + 2 * e + h2;
-            float pv = ex2_approx(fmaf(__uint_as_float(sv[2 * e + h2]), p.c, -lse2[col]));
-            if (diag && col < r) pv = 0.0f;
-            pp[h2] = pv;
-            ds[h2] = pv * (__uint_as_float(dpv[2 * e + h2]) - dd[col]);
+            const int jj = 4 * e + 2 * h2;
+            const uint64_t x = ffma2(f32x2_pack(__uint_as_float(sv[jj]), __uint_as_float(sv[jj + 1])),
+                                     c2, h2 ? f32x2_pack(nl.z, nl.w) : f32x2_pack(nl.x, nl.y));
+            float x0, x1;
+            f32x2_unpack(x, x0, x1);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            if (diag) {
+              if (col0 + jj < r) p0 = 0.0f;
+              if (col0 + jj + 1 < r) p1 = 0.0f;
+            }
+            const uint64_t pp = f32x2_pack(p0, p1);
+            const uint64_t dd = fadd2(
+                f32x2_pack(__uint_as_float(dpv[jj]), __uint_as_float(dpv[jj + 1])),
+                h2 ? f32x2_pack(nd.z, nd.w) : f32x2_pack(nd.x, nd.y));
+            float d0, d1;
+            f32x2_unpack(fmul2(pp, dd), d0, d1);
+            pk[jj / 2] = pack_bf16x2(p0, p1);
+            dk[jj / 2] = pack_bf16x2(d0, d1);
           }
-          pk[e] = pack_bf16x2(pp[0], pp[1]);
-          dk[e] = pack_bf16x2(ds[0], ds[1]);
         }
-        tmem_st16(lane_base + 16 * c, pk);            // P^T over the consumed S^T columns
-        tmem_st16(lane_base + 128 + 16 * c, dk);      // dS^T over the consumed dP^T columns
+        // P^T and dS^T over this warpgroup's consumed S^T / dP^T columns
+        tmem_st16(lane_base + cw * kCols + 16 * c, pk);
+        tmem_st16(lane_base + 128 + cw * kCols + 16 * c, dk);
       }
       tmem_wait_st();
       tc_fence_before_sync();
@@ -356,8 +393,13 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       const int row = j * kT + r;
       const bool valid = row < p.L;
       const size_t off = ((static_cast<size_t>(b) * p.L + row) * p.n_kv + kvh) * kD;
-      store_row(lane_base + 256, p.dv + off, 1.0f, valid);
-      store_row(lane_base + 384, p.dk + off, p.scale, valid);
+      // 8 chunks of 32 columns (dV then dK) shared out over the warpgroups
+#pragma unroll 1
+      for (int q = cw * (8 / kComputeWGs); q < (cw + 1) * (8 / kComputeWGs); ++q) {
+        const int col = (q & 3) * 32;
+        if (q < 4) store_chunk(lane_base + 256 + col, p.dv + off + col, 1.0f, valid);
+        else store_chunk(lane_base + 384 + col, p.dk + off + col, p.scale, valid);
+      }
     }
   }
   teardown(sy, p, false);
@@ -383,7 +425,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
   const int b = grp / p.n_q, h = grp - b * p.n_q;
   const int kvh = h / p.g;
   const int n = p.causal ? i + 1 : p.T;
-  setup(sy, 128);
+  setup(sy, kComputeThreads);
   const uint32_t tmem = sy.tmem_base;
 
   if (warp == kLoadWarp) {
@@ -431,13 +473,16 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
     if (leader) mma_commit(smem_addr(&sy.done));
     teardown(sy, p, leader);
     return;
-  } else {
-    // compute warpgroup: thread r = query row r of the tile = TMEM lane r
-    const int r = warp * 32 + lane;
+  } else if (warp < 4 * kComputeWGs) {
+    // compute warpgroups: thread r = query row r of the tile = TMEM lane r;
+    // warpgroup cw takes key columns [cw*kCols, cw*kCols + kCols)
+    const int cw = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;
     const int row = i * kT + r;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const size_t srow = (static_cast<size_t>(b) * p.n_q + h) * (p.T * kT) + row;
-    const float lse2 = p.lse2[srow], dd = p.rowdot[srow];
+    const float nl = p.nlse2[srow], nd = p.nrowdot[srow];
+    const uint64_t c2 = f32x2_pack(p.c, p.c), nl2 = f32x2_pack(nl, nl), nd2 = f32x2_pack(nd, nd);
     bool ok = true;
     for (int t = 0; t < n; ++t) {
       if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.s_full), t & 1, sy, p))) {
@@ -449,26 +494,32 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
       const bool masked = p.causal ? (t == i) : (p.L - t * kT < kT);
       const int keep = p.causal ? r : p.L - 1 - t * kT;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < kCols / 32; ++c) {
+        const int col0 = cw * kCols + 32 * c;
         uint32_t sv[32], dpv[32];
-        tmem_ld32(lane_base + 32 * c, sv);
-        tmem_ld32(lane_base + 128 + 32 * c, dpv);
+        tmem_ld32(lane_base + col0, sv);
+        tmem_ld32(lane_base + 128 + col0, dpv);
         tmem_wait_ld(sv);
         tmem_after_wait(dpv);
         uint32_t dk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          float ds[2];
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int col = 32 * c + 2 * e + h2;
-            float pv = ex2_approx(fmaf(__uint_as_float(sv[2 * e + h2]), p.c, -lse2));
-            if (masked && col > keep) pv = 0.0f;
-            ds[h2] = pv * (__uint_as_float(dpv[2 * e + h2]) - dd);
+          const uint64_t x = ffma2(
+              f32x2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), c2, nl2);
+          float x0, x1;
+          f32x2_unpack(x, x0, x1);
+          float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          if (masked) {
+            if (col0 + 2 * e > keep) p0 = 0.0f;
+            if (col0 + 2 * e + 1 > keep) p1 = 0.0f;
           }
-          dk[e] = pack_bf16x2(ds[0], ds[1]);
+          const uint64_t dd = fadd2(
+              f32x2_pack(__uint_as_float(dpv[2 * e]), __uint_as_float(dpv[2 * e + 1])), nd2);
+          float d0, d1;
+          f32x2_unpack(fmul2(f32x2_pack(p0, p1), dd), d0, d1);
+          dk[e] = pack_bf16x2(d0, d1);
         }
-        tmem_st16(lane_base + 16 * c, dk);            // dS over the consumed S columns
+        tmem_st16(lane_base + cw * kCols + 16 * c, dk);   // dS over consumed S columns
       }
       tmem_wait_st();
       tc_fence_before_sync();
@@ -477,7 +528,9 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
     if (ok && __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.done), 0, sy, p))) {
       tc_fence_after_sync();
       const size_t off = ((static_cast<size_t>(b) * p.L + row) * p.n_q + h) * kD;
-      store_row(lane_base + 256, p.dq + off, p.scale, row < p.L);
+#pragma unroll 1
+      for (int q = cw * (4 / kComputeWGs); q < (cw + 1) * (4 / kComputeWGs); ++q)
+        store_chunk(lane_base + 256 + 32 * q, p.dq + off + 32 * q, p.scale, row < p.L);
     }
   }
   teardown(sy, p, false);
@@ -588,10 +641,10 @@ attn_status_t attn_prefill_bwd(const void* q, const void* k, const void* v, cons
   p.causal = causal;
   p.c = scale * kLog2e;
   p.scale = scale;
-  float* lse2 = static_cast<float*>(workspace);
-  float* rowdot = lse2 + B * n_q * T * kT;
-  p.lse2 = lse2;
-  p.rowdot = rowdot;
+  float* nlse2 = static_cast<float*>(workspace);
+  float* nrowdot = nlse2 + B * n_q * T * kT;
+  p.nlse2 = nlse2;
+  p.nrowdot = nrowdot;
   p.dq = static_cast<uint16_t*>(dq);
   p.dk = static_cast<uint16_t*>(dk);
   p.dv = static_cast<uint16_t*>(dv);
@@ -599,7 +652,7 @@ attn_status_t attn_prefill_bwd(const void* q, const void* k, const void* v, cons
 
   const int64_t rows = B * n_q * T * kT;
   rowdot_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, lse2, rowdot,
+      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, nlse2, nrowdot,
       static_cast<int>(B), static_cast<int>(L), n_q, static_cast<int>(T * kT));
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   dkdv_kernel<<<static_cast<unsigned>(B * n_kv * T), kThreads, kDkdvSmem, stream>>>(mq, mk, mv,
