@@ -211,6 +211,11 @@ def attn_device_check(stream=None) -> int:
     return int(_abi.load().attn_device_check(_stream_handle(stream)))
 
 
+def attn_selftest_wait_timeout(spin_cycles: int, stream=None) -> int:
+    """Enqueue the wait-limit diagnostic kernel (raw status of the launch)."""
+    return int(_abi.load().attn_selftest_wait_timeout(int(spin_cycles), _stream_handle(stream)))
+
+
 def attn_prefill_grid_size(B, L, n_q, n_kv, d_h, causal=True) -> int:
     return int(_abi.load().attn_prefill_grid_size(int(B), int(L), int(n_q), int(n_kv), int(d_h),
                                                   int(bool(causal))))

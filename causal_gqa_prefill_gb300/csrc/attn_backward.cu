@@ -10,8 +10,8 @@
 //   dK_j = scale sum_i dS_ij Q_i  dQ_i = scale sum_j dS_ij K_j
 //
 // Three kernels, no atomics:
-//   rowdot  per query row: LSE*log2(e) and D = dO . O, padded to whole
-//           128-row tiles (+inf / 0) so tiles can be fetched with bulk copies;
+//   rowdot  per query row: -LSE*log2(e) and -D = -dO . O, padded to whole
+//           128-row tiles (-inf / 0) so tiles can be fetched with bulk copies;
 //   dkdv    one CTA per (b, K/V head, 128-key tile j): loops over the g query
 //           heads of the group and the query tiles that see tile j; with the
 //           key dimension on the TMEM lanes it computes S^T = K Q^T and
@@ -21,10 +21,15 @@
 //           for the whole group stay in TMEM until the end;
 //   dq      one CTA per (b, query head, 128-row tile i): S = Q K^T and
 //           dP = dO V^T, dS in TMEM, dQ += dS K over the key tiles it sees.
+// Both tile kernels walk their loop in half-steps of 64 score columns (64
+// queries of a query tile in dkdv, 64 keys of a key tile in dq) with two score
+// buffers in TMEM, so the tensor cores compute half-step u+1's scores while
+// the compute warps turn half-step u's into P/dS.
+//
 // Each kernel has a TMA producer warp, an MMA warp (warp-wide loop, one elected
-// issuing lane) and kComputeWGs compute warpgroups that split the columns of
-// each score tile (thread = TMEM lane = tile row; warpgroup w owns columns
-// [w*C, w*C + C), C = 128 / kComputeWGs). A warpgroup writes its bf16 P/dS
+// issuing lane) and kComputeWGs compute warpgroups that split the 64 columns
+// of a half-step (thread = TMEM lane = tile row; warpgroup w owns columns
+// [w*C, w*C + C), C = 64 / kComputeWGs). A warpgroup writes its bf16 P/dS
 // back over the first C/2 of its own, already consumed, fp32 columns, so no
 // warpgroup ever overwrites columns another one still has to read; the
 // products that consume P/dS take their A operand K-step by K-step from there.
@@ -49,8 +54,10 @@ using namespace gb300;
 constexpr int kD = 128;                  // head dimension
 constexpr int kT = 128;                  // rows per query tile and keys per key tile
 constexpr int kTileBytes = kT * kD * 2;  // one bf16 128 x 128 tile (two 64-column chunks)
-constexpr int kComputeWGs = 2;                       // compute warpgroups
-constexpr int kCols = kT / kComputeWGs;                // tile columns per warpgroup
+constexpr int kHalf = 64;                // score columns per half-step
+constexpr int kComputeWGs = 2;           // compute warpgroups
+constexpr int kCols = kHalf / kComputeWGs;   // dK/dV: half-step columns per warpgroup
+constexpr int kColsQ = kT / kComputeWGs;     // dQ: key-tile columns per warpgroup
 constexpr int kComputeThreads = 128 * kComputeWGs;
 constexpr int kLoadWarp = 4 * kComputeWGs, kMmaWarp = kLoadWarp + 1;
 // producer and MMA warps plus two idle warps: registers are granted per
@@ -72,10 +79,14 @@ struct BwdParams {
   int* status;
 };
 
+constexpr int kStages = 3;               // ring of streamed tiles
+
 struct Sync {
-  uint64_t fixed_full;              // the CTA's fixed tiles (K_j, V_j or Q_i, dO_i)
-  uint64_t full[2], empty[2];       // two-stage ring of streamed tiles
-  uint64_t s_full, p_full, done, drain;
+  uint64_t a_ready;                 // the CTA's fixed A operands are in TMEM
+  uint64_t full[kStages], empty[kStages];
+  uint64_t s_full[2], p_full[2];    // scores ready (commit) / P or dS ready (compute threads)
+  uint64_t dp_full, ds_full;        // dkdv: dP^T ready (commit) / dS^T ready (compute threads)
+  uint64_t done, drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -129,44 +140,103 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
 // TMEM column (relative to the score tile's base) holding the bf16 A operand
 // for K step kk (tile columns 16*kk .. 16*kk + 15): warpgroup w packs its
 // columns [w*C, w*C + C) two per 32-bit column starting at column w*C.
+// (C = kCols in the dK/dV kernel, kColsQ in the dQ kernel.)
+template <int C = kCols>
 __host__ __device__ constexpr uint32_t a_col(int kk) {
-  return static_cast<uint32_t>((16 * kk / kCols) * kCols + (16 * kk % kCols) / 2);
+  return static_cast<uint32_t>((16 * kk / C) * C + (16 * kk % C) / 2);
 }
 
-// 128x128x128 product into TMEM, A and B [128 rows x 128] K-major bf16 tiles.
-__device__ __forceinline__ void mma_rows_x_rows(bool leader, uint32_t d_tmem, uint32_t a_smem,
-                                                uint32_t b_smem) {
-  constexpr uint32_t idesc = idesc_bf16_f32(kT, kT, false);
+// Scores of a half-step: D[128 x 64] = A B^T over K = 128 (d), A a fixed
+// [128 x 128] bf16 operand in TMEM (64 columns, two elements per column), B
+// rows b_row0 .. b_row0 + 63 of a [128 rows x 128] K-major tile in shared memory.
+// The descriptor is built once; later K steps add their byte offset / 16 to
+// its start-address field (shared addresses stay below 2^18, so no carry).
+__device__ __forceinline__ void mma_scores(bool leader, uint32_t d_tmem, uint32_t a_tmem,
+                                           uint32_t b_smem, int b_row0) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kT, kHalf, false);
+  // the whole warp runs the loop; the elected lane issues (a converged warp
+  // issues tcgen05.mma faster than a lone lane in a divergent branch)
+  const uint64_t b0 = sdesc_sw128(b_smem + b_row0 * 128, 16, 1024);
 #pragma unroll
   for (int kk = 0; kk < kD / 16; ++kk) {
     const uint32_t off = (kk >> 2) * (kT * 128) + (kk & 3) * 32;
-    const uint64_t a = sdesc_sw128(a_smem + off, 16, 1024);
-    const uint64_t b = sdesc_sw128(b_smem + off, 16, 1024);
-    if (leader) mma_ss(d_tmem, a, b, idesc, kk > 0 ? 1u : 0u);
+    if (leader) mma_ts(d_tmem, a_tmem + 8 * kk, b0 + (off >> 4), idesc, kk > 0 ? 1u : 0u);
   }
 }
 
-// D[tmem] (+)= A[tmem] (128 x 128, bf16 packed two per column) * B, where B is
-// a [128 rows x 128] bf16 tile used MN-major (its rows are the K dimension).
-__device__ __forceinline__ void mma_tmem_x_rows(bool leader, uint32_t d_tmem, uint32_t a_tmem,
-                                                uint32_t b_smem, bool accumulate) {
-  constexpr uint32_t idesc = idesc_bf16_f32(kT, kD, true);
+// This thread's row of a bf16 [B, L, H, 128] tensor into 64 TMEM columns of
+// its lane, as a tcgen05 A operand (column c = elements 2c, 2c+1, the lower in
+// the low half, which is the row's memory order); rows past L become zeros.
+__device__ __forceinline__ void row_to_tmem(uint32_t taddr, const uint16_t* src, bool valid) {
 #pragma unroll
-  for (int kk = 0; kk < kT / 16; ++kk) {
-    const uint64_t b = sdesc_sw128(b_smem + kk * 16 * 128, kT * 128, 1024);
-    if (leader) mma_ts(d_tmem, a_tmem + a_col(kk), b, idesc, (accumulate || kk > 0) ? 1u : 0u);
+  for (int half = 0; half < 2; ++half) {
+    uint32_t w[32];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      uint4 x = make_uint4(0u, 0u, 0u, 0u);
+      if (valid) x = reinterpret_cast<const uint4*>(src)[8 * half + q];
+      w[4 * q] = x.x;
+      w[4 * q + 1] = x.y;
+      w[4 * q + 2] = x.z;
+      w[4 * q + 3] = x.w;
+    }
+    tmem_st32(taddr + 32 * half, w);
   }
 }
 
-__device__ __forceinline__ void setup(Sync& sy, int nfull) {
+// D[128 x 128] (+)= A B over K = 64: A the bf16 P/dS of a half-step in TMEM
+// (a_col layout), B rows b_row0 .. b_row0 + 63 of a [128 rows x 128] tile,
+// used MN-major (its rows are the K dimension).
+__device__ __forceinline__ void mma_accum(bool leader, uint32_t d_tmem, uint32_t a_tmem,
+                                          uint32_t b_smem, int b_row0, bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kT, kD, true);
+  const uint64_t b0 = sdesc_sw128(b_smem + b_row0 * 128, kT * 128, 1024);
+#pragma unroll
+  for (int kk = 0; kk < kHalf / 16; ++kk)
+    if (leader)
+      mma_ts(d_tmem, a_tmem + a_col(kk), b0 + ((kk * 16 * 128) >> 4), idesc,
+             (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// Scores of a whole tile: D[128 x 128] = A B^T over K = 128, A a fixed operand
+// in TMEM, B a [128 rows x 128] K-major tile in shared memory.
+__device__ __forceinline__ void mma_scores_full(bool leader, uint32_t d_tmem, uint32_t a_tmem,
+                                                uint32_t b_smem) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kT, kT, false);
+  const uint64_t b0 = sdesc_sw128(b_smem, 16, 1024);
+#pragma unroll
+  for (int kk = 0; kk < kD / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * (kT * 128) + (kk & 3) * 32;
+    if (leader) mma_ts(d_tmem, a_tmem + 8 * kk, b0 + (off >> 4), idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// D[128 x 128] (+)= A B over K = 128: A the bf16 dS of a whole tile in TMEM
+// (a_col<kColsQ> layout), B a [128 rows x 128] tile used MN-major.
+__device__ __forceinline__ void mma_accum_full(bool leader, uint32_t d_tmem, uint32_t a_tmem,
+                                               uint32_t b_smem, bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kT, kD, true);
+  const uint64_t b0 = sdesc_sw128(b_smem, kT * 128, 1024);
+#pragma unroll
+  for (int kk = 0; kk < kT / 16; ++kk)
+    if (leader)
+      mma_ts(d_tmem, a_tmem + a_col<kColsQ>(kk), b0 + ((kk * 16 * 128) >> 4), idesc,
+             (accumulate || kk > 0) ? 1u : 0u);
+}
+
+__device__ __forceinline__ void setup(Sync& sy) {
   if (threadIdx.x == 0) {
-    mbar_init(smem_addr(&sy.fixed_full), 1);
-    for (int s = 0; s < 2; ++s) {
+    mbar_init(smem_addr(&sy.a_ready), kComputeThreads);
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_addr(&sy.full[s]), 1);
       mbar_init(smem_addr(&sy.empty[s]), 1);
     }
-    mbar_init(smem_addr(&sy.s_full), 1);
-    mbar_init(smem_addr(&sy.p_full), nfull);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_addr(&sy.s_full[s]), 1);
+      mbar_init(smem_addr(&sy.p_full[s]), kComputeThreads);
+    }
+    mbar_init(smem_addr(&sy.dp_full), 1);
+    mbar_init(smem_addr(&sy.ds_full), kComputeThreads);
     mbar_init(smem_addr(&sy.done), 1);
     mbar_init(smem_addr(&sy.drain), 1);
     sy.abort = 0;
@@ -244,17 +314,24 @@ __global__ void rowdot_kernel(const uint16_t* o, const uint16_t* dout, const flo
 
 // -------------------------------------------------------------------- dK, dV
 
+// Producer side shared by both tile kernels: drains the ring so that no copy is
+// still in flight when the CTA exits; `issued` tiles were put in flight.
+__device__ __forceinline__ void drain_ring(Sync& sy, int issued) {
+  for (int s = 0; s < kStages && s < issued; ++s) {
+    const int last = s + ((issued - 1 - s) / kStages) * kStages;
+    wait_drain(smem_addr(&sy.full[s]), (last / kStages) & 1);
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+            const uint16_t* __restrict__ k_rows, const uint16_t* __restrict__ v_rows,
             const BwdParams p) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Sync sy;
-  // smem: K_j | V_j | stage 0: Q, dO, lse2[128], D[128] | stage 1: same
+  // smem: kStages x [Q_i | dO_i | -LSE*log2 e [128] | -D [128]]
   const uint32_t base = (smem_addr(dyn_smem) + 1023u) & ~1023u;
-  const uint32_t sK = base, sV = base + kTileBytes;
   constexpr uint32_t kStage = 2 * kTileBytes + 1024;
-  const uint32_t sStage = base + 2 * kTileBytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int groups = static_cast<int>(gridDim.x) / p.T;
   const int j = blockIdx.x / groups;                  // key tile (ascending = most work first)
@@ -262,28 +339,22 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   const int b = grp / p.n_kv, kvh = grp - b * p.n_kv;
   const int i0 = p.causal ? j : 0;
   const int nsteps = p.g * (p.T - i0);                 // (head, query tile) pairs
-  setup(sy, kComputeThreads);
+  const int nhalf = 2 * nsteps;                        // half-steps of 64 queries
+  setup(sy);
   const uint32_t tmem = sy.tmem_base;
+  // TMEM columns: K_j 0..63 and V_j 64..127 (A operands), S^T 128..191,
+  // dP^T 192..255, dV 256..383, dK 384..511
+  constexpr uint32_t cK = 0, cV = 64, cS = 128, cP = 192, cDV = 256, cDK = 384;
 
   if (warp == kLoadWarp) {
     if (lane == 0) {
-      const uint32_t fb = smem_addr(&sy.fixed_full);
-      mbar_arrive_expect_tx(fb, 2 * kTileBytes);
-      for (int c = 0; c < 2; ++c) {
-        tma_load_4d(sK + c * kT * 128, &tmK, fb, c * 64, kvh, j * kT, b);
-        tma_load_4d(sV + c * kT * 128, &tmV, fb, c * 64, kvh, j * kT, b);
-      }
       int t = 0;
-      bool ok = true;
-      for (; t < nsteps && ok; ++t) {
-        const int st = t & 1, use = t >> 1;
-        if (use > 0 && !wait_bounded(smem_addr(&sy.empty[st]), (use - 1) & 1, sy, p)) {
-          ok = false;
-          break;
-        }
+      for (; t < nsteps; ++t) {
+        const int st = t % kStages, use = t / kStages;
+        if (use > 0 && !wait_bounded(smem_addr(&sy.empty[st]), (use - 1) & 1, sy, p)) break;
         const int h = kvh * p.g + t / (p.T - i0);
         const int i = i0 + t % (p.T - i0);
-        const uint32_t dst = sStage + st * kStage, bar = smem_addr(&sy.full[st]);
+        const uint32_t dst = base + st * kStage, bar = smem_addr(&sy.full[st]);
         mbar_arrive_expect_tx(bar, 2 * kTileBytes + 1024);
         for (int c = 0; c < 2; ++c) {
           tma_load_4d(dst + c * kT * 128, &tmQ, bar, c * 64, h, i * kT, b);
@@ -293,71 +364,96 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         bulk_load(dst + 2 * kTileBytes, p.nlse2 + row0, 512, bar);
         bulk_load(dst + 2 * kTileBytes + 512, p.nrowdot + row0, 512, bar);
       }
-      // let every copy land before the CTA can exit
-      wait_drain(smem_addr(&sy.fixed_full), 0);
-      for (int s = 0; s < 2 && s < t; ++s) {
-        const int last = s + ((t - 1 - s) / 2) * 2;
-        wait_drain(smem_addr(&sy.full[s]), (last >> 1) & 1);
-      }
+      drain_ring(sy, t);
     }
   } else if (warp == kMmaWarp) {
     const bool leader = elect_one();
-    bool ok = __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.fixed_full), 0, sy, p));
+    bool ok = __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.a_ready), 0, sy, p));
     tc_fence_after_sync();
-    for (int t = 0; t < nsteps && ok; ++t) {
-      const int st = t & 1;
-      const uint32_t sQ = sStage + st * kStage, sdO = sQ + kTileBytes;
-      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.full[st]), (t >> 1) & 1, sy, p))) break;
+    // S^T(u) = K Q^T (into cS) and dP^T(u) = V dO^T (into cP) for half-step u
+    auto stage_of = [&](int u) { return base + ((u >> 1) % kStages) * kStage; };
+    auto wait_stage = [&](int u) -> bool {
+      if (u & 1) return true;   // the second half uses the stage the first one waited for
+      const int t = u >> 1;
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.full[t % kStages]),
+                                                (t / kStages) & 1, sy, p)))
+        return false;
       tc_fence_after_sync();
-      mma_rows_x_rows(leader, tmem + 0, sK, sQ);       // S^T  = K Q^T
-      mma_rows_x_rows(leader, tmem + 128, sV, sdO);    // dP^T = V dO^T
-      if (leader) mma_commit(smem_addr(&sy.s_full));
-      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.p_full), t & 1, sy, p))) break;
+      return true;
+    };
+    if (ok && (ok = wait_stage(0))) {
+      mma_scores(leader, tmem + cS, tmem + cK, stage_of(0), 0);
+      if (leader) mma_commit(smem_addr(&sy.s_full[0]));
+      mma_scores(leader, tmem + cP, tmem + cV, stage_of(0) + kTileBytes, 0);
+      if (leader) mma_commit(smem_addr(&sy.dp_full));
+    }
+    for (int u = 0; u < nhalf && ok; ++u) {
+      const uint32_t sQ = stage_of(u), sdO = sQ + kTileBytes;
+      const int r0 = 64 * (u & 1);
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.p_full[0]), u & 1, sy, p))) break;
       tc_fence_after_sync();
-      mma_tmem_x_rows(leader, tmem + 256, tmem + 0, sdO, t > 0);    // dV += P^T dO
-      mma_tmem_x_rows(leader, tmem + 384, tmem + 128, sQ, t > 0);   // dK += dS^T Q
-      if (leader) mma_commit(smem_addr(&sy.empty[st]));
+      mma_accum(leader, tmem + cDV, tmem + cS, sdO, r0, u > 0);            // dV += P^T dO
+      const bool more = u + 1 < nhalf;
+      if (more) {
+        if (!wait_stage(u + 1)) break;
+        mma_scores(leader, tmem + cS, tmem + cK, stage_of(u + 1), 64 * ((u + 1) & 1));
+        if (leader) mma_commit(smem_addr(&sy.s_full[0]));
+      }
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.ds_full), u & 1, sy, p))) break;
+      tc_fence_after_sync();
+      mma_accum(leader, tmem + cDK, tmem + cP, sQ, r0, u > 0);             // dK += dS^T Q
+      if (leader && (u & 1)) mma_commit(smem_addr(&sy.empty[(u >> 1) % kStages]));
+      if (more) {
+        mma_scores(leader, tmem + cP, tmem + cV, stage_of(u + 1) + kTileBytes,
+                   64 * ((u + 1) & 1));
+        if (leader) mma_commit(smem_addr(&sy.dp_full));
+      }
     }
     if (leader) mma_commit(smem_addr(&sy.done));
     teardown(sy, p, leader);
     return;
   } else if (warp < 4 * kComputeWGs) {
     // compute warpgroups: thread r = key row r of the tile = TMEM lane r;
-    // warpgroup cw takes query columns [cw*kCols, cw*kCols + kCols)
+    // warpgroup cw takes query columns [cw*kCols, cw*kCols + kCols) of a half-step
     const int cw = warp >> 2;
     const int r = (warp & 3) * 32 + lane;
+    const int krow = j * kT + r;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    {
+      // K_j (first warpgroup) and V_j (second) become the A operands in TMEM
+      const size_t off = ((static_cast<size_t>(b) * p.L + krow) * p.n_kv + kvh) * kD;
+      if (cw < 2) row_to_tmem(lane_base + (cw ? cV : cK), (cw ? v_rows : k_rows) + off, krow < p.L);
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(smem_addr(&sy.a_ready));
+    }
     const uint64_t c2 = f32x2_pack(p.c, p.c);
     bool ok = true;
-    for (int t = 0; t < nsteps; ++t) {
-      const int st = t & 1;
+    for (int u = 0; u < nhalf; ++u) {
+      const int t = u >> 1, st = t % kStages;
       const int i = i0 + t % (p.T - i0);
-      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.s_full), t & 1, sy, p))) {
-        ok = false;
-        break;
-      }
-      // the staged row statistics arrived with the stage's copies
-      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.full[st]), (t >> 1) & 1, sy, p))) {
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.s_full[0]), u & 1, sy, p)) ||
+          // the staged row statistics arrived with the stage's copies
+          !__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.full[st]), (t / kStages) & 1, sy, p))) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
+      const int q0 = 64 * (u & 1) + cw * kCols;        // first query column (in the tile)
       const float4* nl4 = reinterpret_cast<const float4*>(
-          dyn_smem + (sStage + st * kStage + 2 * kTileBytes - smem_addr(dyn_smem)));
+          dyn_smem + (base + st * kStage + 2 * kTileBytes - smem_addr(dyn_smem))) + q0 / 4;
       const float4* nd4 = nl4 + 32;
       const bool diag = p.causal && i == j;           // query c < key r is masked
-#pragma unroll 1
-      for (int c = 0; c < kCols / 32; ++c) {
-        const int col0 = cw * kCols + 32 * c;
-        uint32_t sv[32], dpv[32];
-        tmem_ld32(lane_base + col0, sv);
-        tmem_ld32(lane_base + 128 + col0, dpv);
+      // phase 1: P^T from S^T, kept in registers for phase 2
+      float pr[kCols];
+      {
+        uint32_t sv[32];
+        tmem_ld32(lane_base + cS + cw * kCols, sv);
         tmem_wait_ld(sv);
-        tmem_after_wait(dpv);
-        uint32_t pk[16], dk[16];
+        uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float4 nl = nl4[col0 / 4 + e], nd = nd4[col0 / 4 + e];
+          const float4 nl = nl4[e];
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
             const int jj = 4 * e + 2 * h2;
@@ -367,38 +463,60 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             f32x2_unpack(x, x0, x1);
             float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
             if (diag) {
-              if (col0 + jj < r) p0 = 0.0f;
-              if (col0 + jj + 1 < r) p1 = 0.0f;
+              if (q0 + jj < r) p0 = 0.0f;
+              if (q0 + jj + 1 < r) p1 = 0.0f;
             }
-            const uint64_t pp = f32x2_pack(p0, p1);
+            pr[jj] = p0;
+            pr[jj + 1] = p1;
+            pk[jj / 2] = pack_bf16x2(p0, p1);
+          }
+        }
+        tmem_st16(lane_base + cS + cw * kCols, pk);   // over this warpgroup's consumed S^T columns
+        tmem_wait_st();
+        tc_fence_before_sync();
+        mbar_arrive(smem_addr(&sy.p_full[0]));
+      }
+      // phase 2: dS^T = P^T * (dP^T - D)
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.dp_full), u & 1, sy, p))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      {
+        uint32_t dpv[32];
+        tmem_ld32(lane_base + cP + cw * kCols, dpv);
+        tmem_wait_ld(dpv);
+        uint32_t dk[16];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float4 nd = nd4[e];
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int jj = 4 * e + 2 * h2;
             const uint64_t dd = fadd2(
                 f32x2_pack(__uint_as_float(dpv[jj]), __uint_as_float(dpv[jj + 1])),
                 h2 ? f32x2_pack(nd.z, nd.w) : f32x2_pack(nd.x, nd.y));
             float d0, d1;
-            f32x2_unpack(fmul2(pp, dd), d0, d1);
-            pk[jj / 2] = pack_bf16x2(p0, p1);
+            f32x2_unpack(fmul2(f32x2_pack(pr[jj], pr[jj + 1]), dd), d0, d1);
             dk[jj / 2] = pack_bf16x2(d0, d1);
           }
         }
-        // P^T and dS^T over this warpgroup's consumed S^T / dP^T columns
-        tmem_st16(lane_base + cw * kCols + 16 * c, pk);
-        tmem_st16(lane_base + 128 + cw * kCols + 16 * c, dk);
+        tmem_st16(lane_base + cP + cw * kCols, dk);   // over this warpgroup's consumed dP^T columns
+        tmem_wait_st();
+        tc_fence_before_sync();
+        mbar_arrive(smem_addr(&sy.ds_full));
       }
-      tmem_wait_st();
-      tc_fence_before_sync();
-      mbar_arrive(smem_addr(&sy.p_full));
     }
     if (ok && __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.done), 0, sy, p))) {
       tc_fence_after_sync();
-      const int row = j * kT + r;
-      const bool valid = row < p.L;
-      const size_t off = ((static_cast<size_t>(b) * p.L + row) * p.n_kv + kvh) * kD;
+      const bool valid = krow < p.L;
+      const size_t off = ((static_cast<size_t>(b) * p.L + krow) * p.n_kv + kvh) * kD;
       // 8 chunks of 32 columns (dV then dK) shared out over the warpgroups
 #pragma unroll 1
       for (int q = cw * (8 / kComputeWGs); q < (cw + 1) * (8 / kComputeWGs); ++q) {
         const int col = (q & 3) * 32;
-        if (q < 4) store_chunk(lane_base + 256 + col, p.dv + off + col, 1.0f, valid);
-        else store_chunk(lane_base + 384 + col, p.dk + off + col, p.scale, valid);
+        if (q < 4) store_chunk(lane_base + cDV + col, p.dv + off + col, 1.0f, valid);
+        else store_chunk(lane_base + cDK + col, p.dk + off + col, p.scale, valid);
       }
     }
   }
@@ -408,84 +526,104 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
 // ------------------------------------------------------------------------ dQ
 
 __global__ void __launch_bounds__(kThreads, 1)
-dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+          const uint16_t* __restrict__ q_rows, const uint16_t* __restrict__ do_rows,
           const BwdParams p) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Sync sy;
-  // smem: Q_i | dO_i | stage 0: K_j, V_j | stage 1: K_j, V_j
+  // smem: kStages x [K_t | V_t]
   const uint32_t base = (smem_addr(dyn_smem) + 1023u) & ~1023u;
-  const uint32_t sQ = base, sdO = base + kTileBytes;
   constexpr uint32_t kStage = 2 * kTileBytes;
-  const uint32_t sStage = base + 2 * kTileBytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int groups = static_cast<int>(gridDim.x) / p.T;   // B * n_q
   const int i = p.T - 1 - static_cast<int>(blockIdx.x) / groups;   // longest first
   const int grp = blockIdx.x - (p.T - 1 - i) * groups;
   const int b = grp / p.n_q, h = grp - b * p.n_q;
   const int kvh = h / p.g;
-  const int n = p.causal ? i + 1 : p.T;
-  setup(sy, kComputeThreads);
+  const int n = p.causal ? i + 1 : p.T;                // key tiles
+  setup(sy);
   const uint32_t tmem = sy.tmem_base;
+  // TMEM columns: Q_i 0..63 and dO_i 64..127 (A operands), S 128..255,
+  // dP 256..383 (dS is written over it), dQ 384..511. Per key tile t the
+  // tensor cores run S(t+1) while the compute warps finish dS(t), and dQ(t)
+  // plus dP(t+1) while they turn S(t+1) into P(t+1).
+  constexpr uint32_t cQ = 0, cO = 64, cS = 128, cP = 256, cDQ = 384;
 
   if (warp == kLoadWarp) {
     if (lane == 0) {
-      const uint32_t fb = smem_addr(&sy.fixed_full);
-      mbar_arrive_expect_tx(fb, 2 * kTileBytes);
-      for (int c = 0; c < 2; ++c) {
-        tma_load_4d(sQ + c * kT * 128, &tmQ, fb, c * 64, h, i * kT, b);
-        tma_load_4d(sdO + c * kT * 128, &tmdO, fb, c * 64, h, i * kT, b);
-      }
       int t = 0;
       for (; t < n; ++t) {
-        const int st = t & 1, use = t >> 1;
+        const int st = t % kStages, use = t / kStages;
         if (use > 0 && !wait_bounded(smem_addr(&sy.empty[st]), (use - 1) & 1, sy, p)) break;
-        const uint32_t dst = sStage + st * kStage, bar = smem_addr(&sy.full[st]);
+        const uint32_t dst = base + st * kStage, bar = smem_addr(&sy.full[st]);
         mbar_arrive_expect_tx(bar, 2 * kTileBytes);
         for (int c = 0; c < 2; ++c) {
           tma_load_4d(dst + c * kT * 128, &tmK, bar, c * 64, kvh, t * kT, b);
           tma_load_4d(dst + kTileBytes + c * kT * 128, &tmV, bar, c * 64, kvh, t * kT, b);
         }
       }
-      wait_drain(smem_addr(&sy.fixed_full), 0);
-      for (int s = 0; s < 2 && s < t; ++s) {
-        const int last = s + ((t - 1 - s) / 2) * 2;
-        wait_drain(smem_addr(&sy.full[s]), (last >> 1) & 1);
-      }
+      drain_ring(sy, t);
     }
   } else if (warp == kMmaWarp) {
     const bool leader = elect_one();
-    bool ok = __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.fixed_full), 0, sy, p));
+    bool ok = __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.a_ready), 0, sy, p));
     tc_fence_after_sync();
+    auto stage_of = [&](int t) { return base + (t % kStages) * kStage; };
+    auto wait_stage = [&](int t) -> bool {
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.full[t % kStages]),
+                                                (t / kStages) & 1, sy, p)))
+        return false;
+      tc_fence_after_sync();
+      return true;
+    };
+    if (ok && (ok = wait_stage(0))) {
+      mma_scores_full(leader, tmem + cS, tmem + cQ, stage_of(0));               // S  = Q K^T
+      if (leader) mma_commit(smem_addr(&sy.s_full[0]));
+      mma_scores_full(leader, tmem + cP, tmem + cO, stage_of(0) + kTileBytes);  // dP = dO V^T
+      if (leader) mma_commit(smem_addr(&sy.dp_full));
+    }
     for (int t = 0; t < n && ok; ++t) {
-      const int st = t & 1;
-      const uint32_t sK = sStage + st * kStage, sV = sK + kTileBytes;
-      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.full[st]), (t >> 1) & 1, sy, p))) break;
+      const bool more = t + 1 < n;
+      // S(t) consumed: the next tile's scores may overwrite it
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.p_full[0]), t & 1, sy, p))) break;
+      if (more) {
+        if (!wait_stage(t + 1)) break;
+        mma_scores_full(leader, tmem + cS, tmem + cQ, stage_of(t + 1));
+        if (leader) mma_commit(smem_addr(&sy.s_full[0]));
+      }
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.ds_full), t & 1, sy, p))) break;
       tc_fence_after_sync();
-      mma_rows_x_rows(leader, tmem + 0, sQ, sK);       // S  = Q K^T
-      mma_rows_x_rows(leader, tmem + 128, sdO, sV);    // dP = dO V^T
-      if (leader) mma_commit(smem_addr(&sy.s_full));
-      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.p_full), t & 1, sy, p))) break;
-      tc_fence_after_sync();
-      mma_tmem_x_rows(leader, tmem + 256, tmem + 0, sK, t > 0);     // dQ += dS K
-      if (leader) mma_commit(smem_addr(&sy.empty[st]));
+      mma_accum_full(leader, tmem + cDQ, tmem + cP, stage_of(t), t > 0);        // dQ += dS K
+      if (leader) mma_commit(smem_addr(&sy.empty[t % kStages]));
+      if (more) {
+        mma_scores_full(leader, tmem + cP, tmem + cO, stage_of(t + 1) + kTileBytes);
+        if (leader) mma_commit(smem_addr(&sy.dp_full));
+      }
     }
     if (leader) mma_commit(smem_addr(&sy.done));
     teardown(sy, p, leader);
     return;
   } else if (warp < 4 * kComputeWGs) {
     // compute warpgroups: thread r = query row r of the tile = TMEM lane r;
-    // warpgroup cw takes key columns [cw*kCols, cw*kCols + kCols)
+    // warpgroup cw takes key columns [cw*kColsQ, cw*kColsQ + kColsQ)
     const int cw = warp >> 2;
     const int r = (warp & 3) * 32 + lane;
     const int row = i * kT + r;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const size_t qoff = ((static_cast<size_t>(b) * p.L + row) * p.n_q + h) * kD;
+    // Q_i (first warpgroup) and dO_i (second) become the A operands in TMEM
+    if (cw < 2) row_to_tmem(lane_base + (cw ? cO : cQ), (cw ? do_rows : q_rows) + qoff, row < p.L);
+    tmem_wait_st();
+    tc_fence_before_sync();
+    mbar_arrive(smem_addr(&sy.a_ready));
     const size_t srow = (static_cast<size_t>(b) * p.n_q + h) * (p.T * kT) + row;
     const float nl = p.nlse2[srow], nd = p.nrowdot[srow];
     const uint64_t c2 = f32x2_pack(p.c, p.c), nl2 = f32x2_pack(nl, nl), nd2 = f32x2_pack(nd, nd);
+    const int k0 = cw * kColsQ;                        // first key column (in the tile)
     bool ok = true;
     for (int t = 0; t < n; ++t) {
-      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.s_full), t & 1, sy, p))) {
+      // phase 1: P from S, kept in registers
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.s_full[0]), t & 1, sy, p))) {
         ok = false;
         break;
       }
@@ -493,15 +631,12 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
       // keys after `keep` (in-tile) are masked: the diagonal tile, or keys past L
       const bool masked = p.causal ? (t == i) : (p.L - t * kT < kT);
       const int keep = p.causal ? r : p.L - 1 - t * kT;
-#pragma unroll 1
-      for (int c = 0; c < kCols / 32; ++c) {
-        const int col0 = cw * kCols + 32 * c;
-        uint32_t sv[32], dpv[32];
-        tmem_ld32(lane_base + col0, sv);
-        tmem_ld32(lane_base + 128 + col0, dpv);
+      float pr[kColsQ];
+#pragma unroll
+      for (int c = 0; c < kColsQ / 32; ++c) {
+        uint32_t sv[32];
+        tmem_ld32(lane_base + cS + k0 + 32 * c, sv);
         tmem_wait_ld(sv);
-        tmem_after_wait(dpv);
-        uint32_t dk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const uint64_t x = ffma2(
@@ -510,27 +645,46 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
           f32x2_unpack(x, x0, x1);
           float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
           if (masked) {
-            if (col0 + 2 * e > keep) p0 = 0.0f;
-            if (col0 + 2 * e + 1 > keep) p1 = 0.0f;
+            if (k0 + 32 * c + 2 * e > keep) p0 = 0.0f;
+            if (k0 + 32 * c + 2 * e + 1 > keep) p1 = 0.0f;
           }
+          pr[32 * c + 2 * e] = p0;
+          pr[32 * c + 2 * e + 1] = p1;
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(smem_addr(&sy.p_full[0]));
+      // phase 2: dS = P * (dP - D), written over this warpgroup's consumed dP columns
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.dp_full), t & 1, sy, p))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+#pragma unroll
+      for (int c = 0; c < kColsQ / 32; ++c) {
+        uint32_t dpv[32];
+        tmem_ld32(lane_base + cP + k0 + 32 * c, dpv);
+        tmem_wait_ld(dpv);
+        uint32_t dk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
           const uint64_t dd = fadd2(
               f32x2_pack(__uint_as_float(dpv[2 * e]), __uint_as_float(dpv[2 * e + 1])), nd2);
           float d0, d1;
-          f32x2_unpack(fmul2(f32x2_pack(p0, p1), dd), d0, d1);
+          f32x2_unpack(fmul2(f32x2_pack(pr[32 * c + 2 * e], pr[32 * c + 2 * e + 1]), dd), d0, d1);
           dk[e] = pack_bf16x2(d0, d1);
         }
-        tmem_st16(lane_base + cw * kCols + 16 * c, dk);   // dS over consumed S columns
+        tmem_st16(lane_base + cP + k0 + 16 * c, dk);
       }
       tmem_wait_st();
       tc_fence_before_sync();
-      mbar_arrive(smem_addr(&sy.p_full));
+      mbar_arrive(smem_addr(&sy.ds_full));
     }
     if (ok && __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.done), 0, sy, p))) {
       tc_fence_after_sync();
-      const size_t off = ((static_cast<size_t>(b) * p.L + row) * p.n_q + h) * kD;
 #pragma unroll 1
       for (int q = cw * (4 / kComputeWGs); q < (cw + 1) * (4 / kComputeWGs); ++q)
-        store_chunk(lane_base + 256 + 32 * q, p.dq + off + 32 * q, p.scale, row < p.L);
+        store_chunk(lane_base + cDQ + 32 * q, p.dq + qoff + 32 * q, p.scale, row < p.L);
     }
   }
   teardown(sy, p, false);
@@ -546,8 +700,8 @@ constexpr int kMaxDevices = 64;
 std::mutex g_bwd_mutex;
 bool g_bwd_ready[kMaxDevices];
 EncodeTiledFn g_bwd_encode = nullptr;
-constexpr int kDkdvSmem = 2 * kTileBytes + 2 * (2 * kTileBytes + 1024) + 1024;
-constexpr int kDqSmem = 2 * kTileBytes + 2 * (2 * kTileBytes) + 1024;
+constexpr int kDkdvSmem = kStages * (2 * kTileBytes + 1024) + 1024;
+constexpr int kDqSmem = kStages * (2 * kTileBytes) + 1024;
 
 attn_status_t bwd_device_ready(cudaStream_t stream, int** status) {
   int dev = 0;
@@ -655,10 +809,14 @@ attn_status_t attn_prefill_bwd(const void* q, const void* k, const void* v, cons
       static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, nlse2, nrowdot,
       static_cast<int>(B), static_cast<int>(L), n_q, static_cast<int>(T * kT));
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-  dkdv_kernel<<<static_cast<unsigned>(B * n_kv * T), kThreads, kDkdvSmem, stream>>>(mq, mk, mv,
-                                                                                     mdo, p);
+  const uint16_t* qh = static_cast<const uint16_t*>(q);
+  const uint16_t* kh = static_cast<const uint16_t*>(k);
+  const uint16_t* vh = static_cast<const uint16_t*>(v);
+  const uint16_t* doh = static_cast<const uint16_t*>(dout);
+  dkdv_kernel<<<static_cast<unsigned>(B * n_kv * T), kThreads, kDkdvSmem, stream>>>(mq, mdo, kh,
+                                                                                     vh, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-  dq_kernel<<<static_cast<unsigned>(B * n_q * T), kThreads, kDqSmem, stream>>>(mq, mk, mv, mdo, p);
+  dq_kernel<<<static_cast<unsigned>(B * n_q * T), kThreads, kDqSmem, stream>>>(mk, mv, qh, doh, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -192,6 +192,25 @@ __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, Ctl& ctl
   return __all_sync(0xffffffffu, wait_phase(bar, parity, ctl, p));
 }
 
+// Diagnostic kernel for the wait limit: warp 0 waits on an mbarrier that
+// nothing ever completes and must give up after p.spin_limit cycles, raising
+// the abort flag and the device status word; warp 1 waits on a second such
+// barrier and must leave through the abort flag (or its own limit). Both use
+// the same wait routine as the attention roles.
+__global__ void __launch_bounds__(64, 1) wait_selftest_kernel(const Params p) {
+  __shared__ Ctl ctl;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&ctl.q_full), 1);
+    mbar_init(smem_addr(&ctl.q_empty), 1);
+    ctl.abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const uint32_t bar = smem_addr((threadIdx.x >> 5) == 0 ? &ctl.q_full : &ctl.q_empty);
+  wait_all(bar, 0, ctl, p);
+  __syncthreads();
+}
+
 // ------------------------------------------------------------------ producer
 
 template <int D, bool F8>
@@ -865,6 +884,19 @@ attn_status_t attn_device_check(void* stream_ptr) {
   if (word == 0) return ATTN_OK;
   if (cudaMemset(status, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_ERR_TIMEOUT;
+}
+
+attn_status_t attn_selftest_wait_timeout(int64_t spin_cycles, void* stream_ptr) {
+  if (spin_cycles < 1 || spin_cycles > kSpinLimitCycles) return ATTN_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  DeviceState* st = nullptr;
+  const attn_status_t ds = device_state(stream, &st);
+  if (ds != ATTN_OK) return ds;
+  Params p{};
+  p.status = st->status;
+  p.spin_limit = spin_cycles;
+  wait_selftest_kernel<<<1, 64, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int64_t attn_prefill_grid_size(int64_t B, int64_t L, int32_t n_q, int32_t n_kv, int32_t d_h,

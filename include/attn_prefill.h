@@ -1,6 +1,7 @@
 /*
- * attn_prefill.h — C ABI of the GB300 (sm_103a) causal GQA prefill attention
- * forward pass.
+ * attn_prefill.h — C ABI of the GB300 (sm_103a) causal GQA prefill attention:
+ * the forward pass (square and chunked, bf16 and fp8), decode, the backward
+ * pass and two diagnostics.
  *
  * Operation (one call computes, for every batch b, query head h and row i):
  *
@@ -193,6 +194,19 @@ const char* attn_status_string(attn_status_t status);
  * else ATTN_OK.
  */
 attn_status_t attn_device_check(void* stream);
+
+/*
+ * Diagnostic of the device-side wait limit (no counterpart on the pages; it
+ * exists so that the timeout path can be exercised without a fault). Enqueues
+ * one small kernel that runs the attention kernels' bounded wait on an
+ * mbarrier nothing completes, with a limit of spin_cycles SM clock cycles
+ * (1 .. 2^31; ATTN_ERR_INVALID_ARG otherwise): the wait gives up, raises the
+ * kernel's abort flag (a second waiting warp leaves through it) and sets the
+ * device status word, so the next attn_device_check returns ATTN_ERR_TIMEOUT
+ * and clears it. The CUDA context stays usable. Returns ATTN_OK after
+ * enqueueing.
+ */
+attn_status_t attn_selftest_wait_timeout(int64_t spin_cycles, void* stream);
 
 /*
  * Number of persistent CTAs the forward kernel launches for these sizes on

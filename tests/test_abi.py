@@ -148,6 +148,12 @@ def test_backward_workspace_and_validation(lib):
     assert cg.attn_prefill_bwd(*bad, stream=0) == cg.ATTN_ERR_UNSUPPORTED
 
 
+def test_selftest_rejects_bad_limits(lib):
+    assert cg.attn_selftest_wait_timeout(0, stream=0) == cg.ATTN_ERR_INVALID_ARG
+    assert cg.attn_selftest_wait_timeout(-5, stream=0) == cg.ATTN_ERR_INVALID_ARG
+    assert cg.attn_selftest_wait_timeout((1 << 31) + 1, stream=0) == cg.ATTN_ERR_INVALID_ARG
+
+
 def test_chunk_workload_flops_reduce_to_square():
     w = workloads.custom(1, 300, 4, 2, 64, Lk=300)
     assert w.metric_flops() == oflops.causal_attention_flops(1, 300, 4, 64)
