@@ -79,10 +79,12 @@ struct BwdParams {
   int* status;
 };
 
-constexpr int kStages = 3;               // ring of streamed tiles
+constexpr int kStages = 3;               // dQ: ring of streamed K/V tiles
+constexpr int kStagesKV = 2;             // dK/dV: ring of streamed Q/dO tiles (V_j is resident)
 
 struct Sync {
   uint64_t a_ready;                 // the CTA's fixed A operands are in TMEM
+  uint64_t fixed_full;              // dK/dV: V_j has landed in shared memory
   uint64_t full[kStages], empty[kStages];
   uint64_t s_full[2], p_full[2];    // scores ready (commit) / P or dS ready (compute threads)
   uint64_t dp_full, ds_full;        // dkdv: dP^T ready (commit) / dS^T ready (compute threads)
@@ -227,6 +229,7 @@ __device__ __forceinline__ void mma_accum_full(bool leader, uint32_t d_tmem, uin
 __device__ __forceinline__ void setup(Sync& sy) {
   if (threadIdx.x == 0) {
     mbar_init(smem_addr(&sy.a_ready), kComputeThreads);
+    mbar_init(smem_addr(&sy.fixed_full), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_addr(&sy.full[s]), 1);
       mbar_init(smem_addr(&sy.empty[s]), 1);
@@ -316,21 +319,37 @@ __global__ void rowdot_kernel(const uint16_t* o, const uint16_t* dout, const flo
 
 // Producer side shared by both tile kernels: drains the ring so that no copy is
 // still in flight when the CTA exits; `issued` tiles were put in flight.
+template <int S>
 __device__ __forceinline__ void drain_ring(Sync& sy, int issued) {
-  for (int s = 0; s < kStages && s < issued; ++s) {
-    const int last = s + ((issued - 1 - s) / kStages) * kStages;
-    wait_drain(smem_addr(&sy.full[s]), (last / kStages) & 1);
+  for (int s = 0; s < S && s < issued; ++s) {
+    const int last = s + ((issued - 1 - s) / S) * S;
+    wait_drain(smem_addr(&sy.full[s]), (last / S) & 1);
+  }
+}
+
+// SS product for dP^T of a half-step: D[128 x 64] = V_j dO^T over K = 128 (d),
+// both operands K-major tiles in shared memory (B rows b_row0 .. b_row0 + 63).
+__device__ __forceinline__ void mma_scores_ss(bool leader, uint32_t d_tmem, uint32_t a_smem,
+                                              uint32_t b_smem, int b_row0) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kT, kHalf, false);
+  const uint64_t a0 = sdesc_sw128(a_smem, 16, 1024);
+  const uint64_t b0 = sdesc_sw128(b_smem + b_row0 * 128, 16, 1024);
+#pragma unroll
+  for (int kk = 0; kk < kD / 16; ++kk) {
+    const uint32_t off = ((kk >> 2) * (kT * 128) + (kk & 3) * 32) >> 4;
+    if (leader) mma_ss(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
 dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
-            const uint16_t* __restrict__ k_rows, const uint16_t* __restrict__ v_rows,
+            const __grid_constant__ CUtensorMap tmV, const uint16_t* __restrict__ k_rows,
             const BwdParams p) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Sync sy;
-  // smem: kStages x [Q_i | dO_i | -LSE*log2 e [128] | -D [128]]
+  // smem: V_j | kStagesKV x [Q_i | dO_i | -LSE*log2 e [128] | -D [128]]
   const uint32_t base = (smem_addr(dyn_smem) + 1023u) & ~1023u;
+  const uint32_t sV = base, sRing = base + kTileBytes;
   constexpr uint32_t kStage = 2 * kTileBytes + 1024;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int groups = static_cast<int>(gridDim.x) / p.T;
@@ -342,19 +361,24 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   const int nhalf = 2 * nsteps;                        // half-steps of 64 queries
   setup(sy);
   const uint32_t tmem = sy.tmem_base;
-  // TMEM columns: K_j 0..63 and V_j 64..127 (A operands), S^T 128..191,
-  // dP^T 192..255, dV 256..383, dK 384..511
-  constexpr uint32_t cK = 0, cV = 64, cS = 128, cP = 192, cDV = 256, cDK = 384;
+  // TMEM columns: K_j 0..63 (A operand), S^T of half-step u in buffer u&1 at
+  // 64 + 64*(u&1) (P^T is written over it), dP^T 192..255 (dS^T over it),
+  // dV 256..383, dK 384..511. With two S^T buffers the tensor cores compute
+  // S^T(u+1) while the compute warps are still on half-step u.
+  constexpr uint32_t cK = 0, cS = 64, cP = 192, cDV = 256, cDK = 384;
 
   if (warp == kLoadWarp) {
     if (lane == 0) {
+      const uint32_t fb = smem_addr(&sy.fixed_full);
+      mbar_arrive_expect_tx(fb, kTileBytes);
+      for (int c = 0; c < 2; ++c) tma_load_4d(sV + c * kT * 128, &tmV, fb, c * 64, kvh, j * kT, b);
       int t = 0;
       for (; t < nsteps; ++t) {
-        const int st = t % kStages, use = t / kStages;
+        const int st = t % kStagesKV, use = t / kStagesKV;
         if (use > 0 && !wait_bounded(smem_addr(&sy.empty[st]), (use - 1) & 1, sy, p)) break;
         const int h = kvh * p.g + t / (p.T - i0);
         const int i = i0 + t % (p.T - i0);
-        const uint32_t dst = base + st * kStage, bar = smem_addr(&sy.full[st]);
+        const uint32_t dst = sRing + st * kStage, bar = smem_addr(&sy.full[st]);
         mbar_arrive_expect_tx(bar, 2 * kTileBytes + 1024);
         for (int c = 0; c < 2; ++c) {
           tma_load_4d(dst + c * kT * 128, &tmQ, bar, c * 64, h, i * kT, b);
@@ -364,50 +388,58 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         bulk_load(dst + 2 * kTileBytes, p.nlse2 + row0, 512, bar);
         bulk_load(dst + 2 * kTileBytes + 512, p.nrowdot + row0, 512, bar);
       }
-      drain_ring(sy, t);
+      wait_drain(fb, 0);
+      drain_ring<kStagesKV>(sy, t);
     }
   } else if (warp == kMmaWarp) {
     const bool leader = elect_one();
-    bool ok = __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.a_ready), 0, sy, p));
+    bool ok = __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.a_ready), 0, sy, p)) &&
+              __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.fixed_full), 0, sy, p));
     tc_fence_after_sync();
-    // S^T(u) = K Q^T (into cS) and dP^T(u) = V dO^T (into cP) for half-step u
-    auto stage_of = [&](int u) { return base + ((u >> 1) % kStages) * kStage; };
+    auto stage_of = [&](int u) { return sRing + ((u >> 1) % kStagesKV) * kStage; };
     auto wait_stage = [&](int u) -> bool {
       if (u & 1) return true;   // the second half uses the stage the first one waited for
       const int t = u >> 1;
-      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.full[t % kStages]),
-                                                (t / kStages) & 1, sy, p)))
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.full[t % kStagesKV]),
+                                                (t / kStagesKV) & 1, sy, p)))
         return false;
       tc_fence_after_sync();
       return true;
     };
-    if (ok && (ok = wait_stage(0))) {
-      mma_scores(leader, tmem + cS, tmem + cK, stage_of(0), 0);
-      if (leader) mma_commit(smem_addr(&sy.s_full[0]));
-      mma_scores(leader, tmem + cP, tmem + cV, stage_of(0) + kTileBytes, 0);
+    auto issue_st = [&](int u) {      // S^T(u) = K Q^T into buffer u&1
+      mma_scores(leader, tmem + cS + 64 * (u & 1), tmem + cK, stage_of(u), 64 * (u & 1));
+      if (leader) mma_commit(smem_addr(&sy.s_full[u & 1]));
+    };
+    auto issue_dpt = [&](int u) {     // dP^T(u) = V dO^T
+      mma_scores_ss(leader, tmem + cP, sV, stage_of(u) + kTileBytes, 64 * (u & 1));
       if (leader) mma_commit(smem_addr(&sy.dp_full));
+    };
+    if (ok && (ok = wait_stage(0))) {
+      issue_st(0);
+      issue_dpt(0);
     }
     for (int u = 0; u < nhalf && ok; ++u) {
       const uint32_t sQ = stage_of(u), sdO = sQ + kTileBytes;
       const int r0 = 64 * (u & 1);
-      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.p_full[0]), u & 1, sy, p))) break;
-      tc_fence_after_sync();
-      mma_accum(leader, tmem + cDV, tmem + cS, sdO, r0, u > 0);            // dV += P^T dO
       const bool more = u + 1 < nhalf;
+      // S^T(u+1) goes into the buffer that held half-step u-1, whose P^T the
+      // previously issued dV(u-1) reads first (the tensor cores run in order)
       if (more) {
         if (!wait_stage(u + 1)) break;
-        mma_scores(leader, tmem + cS, tmem + cK, stage_of(u + 1), 64 * ((u + 1) & 1));
-        if (leader) mma_commit(smem_addr(&sy.s_full[0]));
+        issue_st(u + 1);
       }
+      // one P-ready barrier per S^T buffer: the compute warps may finish P^T(u+1)
+      // before this wait runs, which a single barrier could not tell apart
+      if (!__all_sync(0xffffffffu,
+                      wait_bounded(smem_addr(&sy.p_full[u & 1]), (u >> 1) & 1, sy, p)))
+        break;
+      tc_fence_after_sync();
+      mma_accum(leader, tmem + cDV, tmem + cS + 64 * (u & 1), sdO, r0, u > 0);   // dV += P^T dO
       if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.ds_full), u & 1, sy, p))) break;
       tc_fence_after_sync();
-      mma_accum(leader, tmem + cDK, tmem + cP, sQ, r0, u > 0);             // dK += dS^T Q
-      if (leader && (u & 1)) mma_commit(smem_addr(&sy.empty[(u >> 1) % kStages]));
-      if (more) {
-        mma_scores(leader, tmem + cP, tmem + cV, stage_of(u + 1) + kTileBytes,
-                   64 * ((u + 1) & 1));
-        if (leader) mma_commit(smem_addr(&sy.dp_full));
-      }
+      mma_accum(leader, tmem + cDK, tmem + cP, sQ, r0, u > 0);                   // dK += dS^T Q
+      if (leader && (u & 1)) mma_commit(smem_addr(&sy.empty[(u >> 1) % kStagesKV]));
+      if (more) issue_dpt(u + 1);
     }
     if (leader) mma_commit(smem_addr(&sy.done));
     teardown(sy, p, leader);
@@ -419,36 +451,37 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     const int r = (warp & 3) * 32 + lane;
     const int krow = j * kT + r;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    {
-      // K_j (first warpgroup) and V_j (second) become the A operands in TMEM
-      const size_t off = ((static_cast<size_t>(b) * p.L + krow) * p.n_kv + kvh) * kD;
-      if (cw < 2) row_to_tmem(lane_base + (cw ? cV : cK), (cw ? v_rows : k_rows) + off, krow < p.L);
-      tmem_wait_st();
-      tc_fence_before_sync();
-      mbar_arrive(smem_addr(&sy.a_ready));
-    }
+    // K_j becomes the A operand of S^T in TMEM (first warpgroup)
+    const size_t koff = ((static_cast<size_t>(b) * p.L + krow) * p.n_kv + kvh) * kD;
+    if (cw == 0) row_to_tmem(lane_base + cK, k_rows + koff, krow < p.L);
+    tmem_wait_st();
+    tc_fence_before_sync();
+    mbar_arrive(smem_addr(&sy.a_ready));
     const uint64_t c2 = f32x2_pack(p.c, p.c);
     bool ok = true;
     for (int u = 0; u < nhalf; ++u) {
-      const int t = u >> 1, st = t % kStages;
+      const int t = u >> 1, st = t % kStagesKV;
       const int i = i0 + t % (p.T - i0);
-      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.s_full[0]), u & 1, sy, p)) ||
+      if (!__all_sync(0xffffffffu,
+                      wait_bounded(smem_addr(&sy.s_full[u & 1]), (u >> 1) & 1, sy, p)) ||
           // the staged row statistics arrived with the stage's copies
-          !__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.full[st]), (t / kStages) & 1, sy, p))) {
+          !__all_sync(0xffffffffu,
+                      wait_bounded(smem_addr(&sy.full[st]), (t / kStagesKV) & 1, sy, p))) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
       const int q0 = 64 * (u & 1) + cw * kCols;        // first query column (in the tile)
       const float4* nl4 = reinterpret_cast<const float4*>(
-          dyn_smem + (base + st * kStage + 2 * kTileBytes - smem_addr(dyn_smem))) + q0 / 4;
+          dyn_smem + (sRing + st * kStage + 2 * kTileBytes - smem_addr(dyn_smem))) + q0 / 4;
       const float4* nd4 = nl4 + 32;
       const bool diag = p.causal && i == j;           // query c < key r is masked
+      const uint32_t sbuf = lane_base + cS + 64 * (u & 1) + cw * kCols;
       // phase 1: P^T from S^T, kept in registers for phase 2
       float pr[kCols];
       {
         uint32_t sv[32];
-        tmem_ld32(lane_base + cS + cw * kCols, sv);
+        tmem_ld32(sbuf, sv);
         tmem_wait_ld(sv);
         uint32_t pk[16];
 #pragma unroll
@@ -471,10 +504,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             pk[jj / 2] = pack_bf16x2(p0, p1);
           }
         }
-        tmem_st16(lane_base + cS + cw * kCols, pk);   // over this warpgroup's consumed S^T columns
+        tmem_st16(sbuf, pk);                           // over this warpgroup's consumed S^T columns
         tmem_wait_st();
         tc_fence_before_sync();
-        mbar_arrive(smem_addr(&sy.p_full[0]));
+        mbar_arrive(smem_addr(&sy.p_full[u & 1]));
       }
       // phase 2: dS^T = P^T * (dP^T - D)
       if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.dp_full), u & 1, sy, p))) {
@@ -510,13 +543,12 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     if (ok && __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.done), 0, sy, p))) {
       tc_fence_after_sync();
       const bool valid = krow < p.L;
-      const size_t off = ((static_cast<size_t>(b) * p.L + krow) * p.n_kv + kvh) * kD;
       // 8 chunks of 32 columns (dV then dK) shared out over the warpgroups
 #pragma unroll 1
       for (int q = cw * (8 / kComputeWGs); q < (cw + 1) * (8 / kComputeWGs); ++q) {
         const int col = (q & 3) * 32;
-        if (q < 4) store_chunk(lane_base + cDV + col, p.dv + off + col, 1.0f, valid);
-        else store_chunk(lane_base + cDK + col, p.dk + off + col, p.scale, valid);
+        if (q < 4) store_chunk(lane_base + cDV + col, p.dv + koff + col, 1.0f, valid);
+        else store_chunk(lane_base + cDK + col, p.dk + koff + col, p.scale, valid);
       }
     }
   }
@@ -562,7 +594,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
           tma_load_4d(dst + kTileBytes + c * kT * 128, &tmV, bar, c * 64, kvh, t * kT, b);
         }
       }
-      drain_ring(sy, t);
+      drain_ring<kStages>(sy, t);
     }
   } else if (warp == kMmaWarp) {
     const bool leader = elect_one();
@@ -700,7 +732,7 @@ constexpr int kMaxDevices = 64;
 std::mutex g_bwd_mutex;
 bool g_bwd_ready[kMaxDevices];
 EncodeTiledFn g_bwd_encode = nullptr;
-constexpr int kDkdvSmem = kStages * (2 * kTileBytes + 1024) + 1024;
+constexpr int kDkdvSmem = kTileBytes + kStagesKV * (2 * kTileBytes + 1024) + 1024;
 constexpr int kDqSmem = kStages * (2 * kTileBytes) + 1024;
 
 attn_status_t bwd_device_ready(cudaStream_t stream, int** status) {
@@ -811,10 +843,9 @@ attn_status_t attn_prefill_bwd(const void* q, const void* k, const void* v, cons
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   const uint16_t* qh = static_cast<const uint16_t*>(q);
   const uint16_t* kh = static_cast<const uint16_t*>(k);
-  const uint16_t* vh = static_cast<const uint16_t*>(v);
   const uint16_t* doh = static_cast<const uint16_t*>(dout);
-  dkdv_kernel<<<static_cast<unsigned>(B * n_kv * T), kThreads, kDkdvSmem, stream>>>(mq, mdo, kh,
-                                                                                     vh, p);
+  dkdv_kernel<<<static_cast<unsigned>(B * n_kv * T), kThreads, kDkdvSmem, stream>>>(mq, mdo, mv,
+                                                                                     kh, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   dq_kernel<<<static_cast<unsigned>(B * n_q * T), kThreads, kDqSmem, stream>>>(mk, mv, qh, doh, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
