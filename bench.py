@@ -39,7 +39,6 @@ if ROOT not in sys.path:
 METRIC = "causal prefill attention TFLOP/s (2·n_q·d_h·L²) on 1 GB300; % of bf16 peak"
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
-KERNEL_SOURCE = os.path.join(ROOT, "causal_gqa_prefill_gb300", "csrc", "attn_prefill.cu")
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
@@ -161,24 +160,32 @@ def measured_peaks():
         return {"bf16_tflops": FALLBACK_BF16_TFLOPS}, "fallback"
 
 
-def kernel_source_hash() -> str:
-    with open(KERNEL_SOURCE, "rb") as f:
+def kernel_source(w) -> str:
+    """The CUDA source file that holds the kernels this workload times."""
+    name = ("attn_decode.cu" if w.decode else "attn_backward.cu" if w.backward
+            else "attn_prefill.cu")
+    return os.path.join(ROOT, "causal_gqa_prefill_gb300", "csrc", name)
+
+
+def kernel_source_hash(w) -> str:
+    with open(kernel_source(w), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_traffic(workload_number: int):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (else None)."""
+def recorded_traffic(w):
+    """DRAM bytes per launch (per step for multi-launch steps) from the
+    committed ncu summaries, if they were taken on the current source of this
+    workload's kernels (else None)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    src = kernel_source_hash()
+    src = kernel_source_hash(w)
     with open(path) as f:
         for line in f:
             if line.startswith("#") or not line.strip():
                 continue
             parts = line.split("\t")
-            if len(parts) >= 3 and parts[0] == str(workload_number) and parts[1] == src:
+            if len(parts) >= 3 and parts[0] == str(w.number) and parts[1] == src:
                 return float(parts[2])
     return None
 
@@ -521,7 +528,7 @@ def run_ours(args, w, dist):
     if ratio != 1.0:
         peak_note += " x 2 (nominal e4m3/bf16 tensor-rate ratio)"
     achieved = flops / (statistics.mean(step_ms) * 1e-3) / 1e12
-    traffic = recorded_traffic(w.number)
+    traffic = recorded_traffic(w)
     if w.decode:
         # a decode step is bound by reading the K/V cache once: HBM roofline
         hbm = float(peaks.get("hbm_gbs", 6800.0))
