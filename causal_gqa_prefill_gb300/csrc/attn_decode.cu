@@ -18,7 +18,7 @@
 //                 each lane 8 of the 128 dimensions; head dot products are
 //                 finished with an 8-shuffle butterfly. The CTA writes its
 //                 normalised partial output and log-sum-exp to the workspace.
-//   combine       one warp per (b, query head) merges the S partial results
+//   combine       one CTA per (b, query head) merges the S partial results
 //                 through their log-sum-exps into bf16 O and fp32 LSE.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -327,35 +327,63 @@ attn_decode_split_kernel(const __grid_constant__ CUtensorMap tmK,
   }
 }
 
-// One warp per (b, query head): O = sum_s w_s O_s, w_s = exp(lse_s - LSE).
-__global__ void attn_decode_combine_kernel(const float* part_o, const float* part_lse,
-                                           uint16_t* o, float* lse, int rows, int S) {
-  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
+// One CTA of kCombineWarps warps per (b, query head): O = sum_s w_s O_s,
+// w_s = exp(lse_s - LSE). The warps take interleaved splits (independent
+// loads, so many are in flight at once), each lane four dimensions; the warps'
+// sums are added in shared memory.
+constexpr int kCombineWarps = 8;
+__global__ void __launch_bounds__(32 * kCombineWarps)
+attn_decode_combine_kernel(const float* part_o, const float* part_lse, uint16_t* o, float* lse,
+                           int S) {
+  __shared__ float red_m[kCombineWarps], red_w[kCombineWarps];
+  __shared__ float4 red_o[kCombineWarps][32];
+  const int row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* pl = part_lse + static_cast<size_t>(row) * S;
   float mx = -INFINITY;
-  for (int s = lane; s < S; s += 32) mx = fmaxf(mx, pl[s]);
+  for (int s = threadIdx.x; s < S; s += blockDim.x) mx = fmaxf(mx, pl[s]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  if (lane == 0) red_m[warp] = mx;
+  __syncthreads();
+  mx = red_m[0];
+#pragma unroll
+  for (int w = 1; w < kCombineWarps; ++w) mx = fmaxf(mx, red_m[w]);
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   float wsum = 0.0f;
-  for (int s = 0; s < S; ++s) {
+#pragma unroll 4
+  for (int s = warp; s < S; s += kCombineWarps) {
     const float ls = pl[s];
     const float w = (ls == -INFINITY) ? 0.0f : __expf(ls - mx);
-    wsum += w;
     const float4 v = *reinterpret_cast<const float4*>(part_o + (static_cast<size_t>(row) * S + s) *
                                                                    kDim + 4 * lane);
-    acc[0] = fmaf(w, v.x, acc[0]);
-    acc[1] = fmaf(w, v.y, acc[1]);
-    acc[2] = fmaf(w, v.z, acc[2]);
-    acc[3] = fmaf(w, v.w, acc[3]);
+    wsum += w;
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
   }
-  const float inv = 1.0f / wsum;
-  const uint32_t w0 = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-  const uint32_t w1 = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-  *reinterpret_cast<uint2*>(o + static_cast<size_t>(row) * kDim + 4 * lane) = make_uint2(w0, w1);
-  if (lane == 0) lse[row] = mx + logf(wsum);
+  red_o[warp][lane] = acc;
+  if (lane == 0) red_w[warp] = wsum;
+  __syncthreads();
+  if (warp == 0) {
+    float4 t = red_o[0][lane];
+    float ws = red_w[0];
+#pragma unroll
+    for (int w = 1; w < kCombineWarps; ++w) {
+      const float4 u = red_o[w][lane];
+      t.x += u.x;
+      t.y += u.y;
+      t.z += u.z;
+      t.w += u.w;
+      ws += red_w[w];
+    }
+    const float inv = 1.0f / ws;
+    const uint32_t w0 = pack_bf16x2(t.x * inv, t.y * inv);
+    const uint32_t w1 = pack_bf16x2(t.z * inv, t.w * inv);
+    *reinterpret_cast<uint2*>(o + static_cast<size_t>(row) * kDim + 4 * lane) = make_uint2(w0, w1);
+    if (lane == 0) lse[row] = mx + logf(ws);
+  }
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -494,8 +522,8 @@ attn_status_t attn_decode_fwd(const void* q, const void* k, const void* v, void*
   }
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   const int rows = static_cast<int>(B * n_q);
-  attn_decode_combine_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(
-      p.part_o, p.part_lse, static_cast<uint16_t*>(o), lse, rows, p.S);
+  attn_decode_combine_kernel<<<rows, 32 * kCombineWarps, 0, stream>>>(
+      p.part_o, p.part_lse, static_cast<uint16_t*>(o), lse, p.S);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
