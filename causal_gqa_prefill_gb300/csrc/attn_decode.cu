@@ -184,17 +184,26 @@ attn_decode_split_kernel(const __grid_constant__ CUtensorMap tmK,
   for (int h = 0; h < G; ++h) {
     const uint4 w = *reinterpret_cast<const uint4*>(
         p.q + (static_cast<size_t>(b) * p.n_q + kvh * G + h) * kDim + 8 * L);
-    q[h][0] = bf16_lo(w.x); q[h][1] = bf16_hi(w.x); q[h][2] = bf16_lo(w.y); q[h][3] = bf16_hi(w.y);
-    q[h][4] = bf16_lo(w.z); q[h][5] = bf16_hi(w.z); q[h][6] = bf16_lo(w.w); q[h][7] = bf16_hi(w.w);
+    // scale * log2(e) folded into q: dot products come out in log2 units
+    q[h][0] = bf16_lo(w.x) * p.c; q[h][1] = bf16_hi(w.x) * p.c;
+    q[h][2] = bf16_lo(w.y) * p.c; q[h][3] = bf16_hi(w.y) * p.c;
+    q[h][4] = bf16_lo(w.z) * p.c; q[h][5] = bf16_hi(w.z) * p.c;
+    q[h][6] = bf16_lo(w.w) * p.c; q[h][7] = bf16_hi(w.w) * p.c;
   }
-  float m[G], l[G], o[G][8];
+  constexpr int GP = Pow2<G>::value;
+  // After the butterfly this lane holds the full score of head `mine` (lanes
+  // 16/GP apart share a head); it alone keeps that head's running max and sum
+  // and computes its weight, which the row's lanes then broadcast.
+  int mine = 0;
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    m[h] = -INFINITY;
-    l[h] = 0.0f;
+  for (int h = 0; h < GP; ++h)
+    if (butterfly_owner<GP>(h) == (L & (16 - 16 / GP))) mine = h;
+  float m_own = -INFINITY, l_own = 0.0f;
+  float o[G][8];
+#pragma unroll
+  for (int h = 0; h < G; ++h)
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[h][i] = 0.0f;
-  }
 
   for (int t = 0; t < n_tiles; ++t) {
     const int s = t % kStages;
@@ -214,7 +223,6 @@ attn_decode_split_kernel(const __grid_constant__ CUtensorMap tmK,
                            bf16_lo(kw.z), bf16_hi(kw.z), bf16_lo(kw.w), bf16_hi(kw.w)};
       // partial dot products of this lane's 8 dimensions, all heads (packed
       // pairs of dimensions, folded at the end); heads past G are zero
-      constexpr int GP = Pow2<G>::value;
       float part[GP];
 #pragma unroll
       for (int h = G; h < GP; ++h) part[h] = 0.0f;
@@ -247,25 +255,31 @@ attn_decode_split_kernel(const __grid_constant__ CUtensorMap tmK,
           part[0] += __shfl_xor_sync(0xffffffffu, part[0], off);
         }
       }
-      // every lane of the row gets every head's score (log2-scaled)
-      float x[G];
+      // the owner lane's online-softmax step for its head (log2 units); keys
+      // past this split (or past the cache) get weight 0
+      const float x = part[0];
+      const bool valid = key < k_end && mine < G;
+      const bool grow = valid && x > m_own + kRescale;   // lazy running max: rare after the first keys
+      if (__any_sync(0xffffffffu, grow)) {
+        const float alpha = grow ? ex2_approx(m_own - x) : 1.0f;
+        if (grow) {
+          m_own = x;
+          l_own *= alpha;
+        }
 #pragma unroll
-      for (int h = 0; h < G; ++h)
-        x[h] = __shfl_sync(0xffffffffu, part[0], (half << 4) | butterfly_owner<GP>(h)) * p.c;
-      if (key >= k_end) continue;          // past this split (or past the cache)
+        for (int h = 0; h < G; ++h) {
+          const float ah = __shfl_sync(0xffffffffu, alpha, (half << 4) | butterfly_owner<GP>(h));
+#pragma unroll
+          for (int i = 0; i < 8; ++i) o[h][i] *= ah;
+        }
+      }
+      const float pw_own = valid ? ex2_approx(x - m_own) : 0.0f;
+      l_own += pw_own;
       const float vf[8] = {bf16_lo(vw.x), bf16_hi(vw.x), bf16_lo(vw.y), bf16_hi(vw.y),
                            bf16_lo(vw.z), bf16_hi(vw.z), bf16_lo(vw.w), bf16_hi(vw.w)};
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        if (x[h] > m[h] + kRescale) {      // lazy running max: rare after the first keys
-          const float alpha = ex2_approx(m[h] - x[h]);
-          m[h] = x[h];
-          l[h] *= alpha;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) o[h][i] *= alpha;
-        }
-        const float pw = ex2_approx(x[h] - m[h]);
-        l[h] += pw;
+        const float pw = __shfl_sync(0xffffffffu, pw_own, (half << 4) | butterfly_owner<GP>(h));
         const uint64_t pw2 = f32x2_pack(pw, pw);
 #pragma unroll
         for (int i = 0; i < 8; i += 2) {
@@ -278,6 +292,13 @@ attn_decode_split_kernel(const __grid_constant__ CUtensorMap tmK,
     if (lane == 0) mbar_arrive(smem_addr(&ctl.empty[s]));
   }
 
+  // every lane takes each head's running max and sum from that head's owner
+  float m[G], l[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m[h] = __shfl_sync(0xffffffffu, m_own, (half << 4) | butterfly_owner<GP>(h));
+    l[h] = __shfl_sync(0xffffffffu, l_own, (half << 4) | butterfly_owner<GP>(h));
+  }
   // merge the warp's two rows (lanes L and L+16 hold the same dimensions)
 #pragma unroll
   for (int h = 0; h < G; ++h) {
