@@ -286,32 +286,58 @@ __device__ __forceinline__ void store_chunk(uint32_t taddr, uint16_t* dst, float
 
 // ------------------------------------------------------------------ rowdot
 
+// Half a warp per padded row (b, h, t), t < Lp: 16 lanes x 8 dimensions, with
+// 16-byte loads; a warp takes four rows so that its loads of all four are in
+// flight together. Rows past L get -inf and 0 without touching O or dO.
+constexpr int kRowdotRowsPerWarp = 4;
+__device__ __forceinline__ float dot8_bf16(uint4 a, uint4 d) {
+  float acc = __uint_as_float(a.x << 16) * __uint_as_float(d.x << 16);
+  acc = fmaf(__uint_as_float(a.x & 0xFFFF0000u), __uint_as_float(d.x & 0xFFFF0000u), acc);
+  acc = fmaf(__uint_as_float(a.y << 16), __uint_as_float(d.y << 16), acc);
+  acc = fmaf(__uint_as_float(a.y & 0xFFFF0000u), __uint_as_float(d.y & 0xFFFF0000u), acc);
+  acc = fmaf(__uint_as_float(a.z << 16), __uint_as_float(d.z << 16), acc);
+  acc = fmaf(__uint_as_float(a.z & 0xFFFF0000u), __uint_as_float(d.z & 0xFFFF0000u), acc);
+  acc = fmaf(__uint_as_float(a.w << 16), __uint_as_float(d.w << 16), acc);
+  acc = fmaf(__uint_as_float(a.w & 0xFFFF0000u), __uint_as_float(d.w & 0xFFFF0000u), acc);
+  return acc;
+}
+
 __global__ void rowdot_kernel(const uint16_t* o, const uint16_t* dout, const float* lse,
                               float* nlse2, float* nrowdot, int B, int L, int n_q, int Lp) {
-  // one warp per padded row (b, h, t); t < Lp
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
   const int64_t total = static_cast<int64_t>(B) * n_q * Lp;
-  if (row >= total) return;
-  const int t = static_cast<int>(row % Lp);
-  const int64_t bh = row / Lp;
-  const int h = static_cast<int>(bh % n_q);
-  const int b = static_cast<int>(bh / n_q);
-  float dd = 0.0f;
-  if (t < L) {
-    const size_t off = ((static_cast<size_t>(b) * L + t) * n_q + h) * kD + 4 * lane;
-    const uint2 a = *reinterpret_cast<const uint2*>(o + off);
-    const uint2 d = *reinterpret_cast<const uint2*>(dout + off);
-    dd = __uint_as_float(a.x << 16) * __uint_as_float(d.x << 16) +
-         __uint_as_float(a.x & 0xFFFF0000u) * __uint_as_float(d.x & 0xFFFF0000u) +
-         __uint_as_float(a.y << 16) * __uint_as_float(d.y << 16) +
-         __uint_as_float(a.y & 0xFFFF0000u) * __uint_as_float(d.y & 0xFFFF0000u);
+  const int64_t warp_id = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int half = (threadIdx.x >> 4) & 1, l16 = threadIdx.x & 15;
+  uint4 a[kRowdotRowsPerWarp / 2], d[kRowdotRowsPerWarp / 2];
+  bool live[kRowdotRowsPerWarp / 2];
+#pragma unroll
+  for (int k = 0; k < kRowdotRowsPerWarp / 2; ++k) {
+    const int64_t row = warp_id * kRowdotRowsPerWarp + 2 * k + half;
+    live[k] = false;
+    a[k] = d[k] = make_uint4(0u, 0u, 0u, 0u);
+    if (row < total) {
+      const int t = static_cast<int>(row % Lp);
+      const int64_t bh = row / Lp;
+      if (t < L) {
+        const int h = static_cast<int>(bh % n_q);
+        const int b = static_cast<int>(bh / n_q);
+        const size_t off = ((static_cast<size_t>(b) * L + t) * n_q + h) * kD + 8 * l16;
+        a[k] = *reinterpret_cast<const uint4*>(o + off);
+        d[k] = *reinterpret_cast<const uint4*>(dout + off);
+        live[k] = true;
+      }
+    }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, off);
-  if (lane == 0) {
-    nrowdot[row] = -dd;
-    nlse2[row] = (t < L) ? -lse[bh * L + t] * kLog2e : -INFINITY;
+  for (int k = 0; k < kRowdotRowsPerWarp / 2; ++k) {
+    float dd = live[k] ? dot8_bf16(a[k], d[k]) : 0.0f;
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, off);
+    const int64_t row = warp_id * kRowdotRowsPerWarp + 2 * k + half;
+    if (l16 == 0 && row < total) {
+      const int t = static_cast<int>(row % Lp);
+      nrowdot[row] = -dd;
+      nlse2[row] = (t < L) ? -lse[(row / Lp) * L + t] * kLog2e : -INFINITY;
+    }
   }
 }
 
@@ -805,7 +831,8 @@ attn_status_t attn_prefill_bwd(const void* q, const void* k, const void* v, cons
     return ATTN_ERR_INVALID_ARG;
   if (d_h != kD) return ATTN_ERR_UNSUPPORTED;
   const int64_t T = (L + kT - 1) / kT;
-  if (L > (int64_t{1} << 30) || B * n_kv * T > INT32_MAX || B * n_q * T > INT32_MAX)
+  // 32-bit tile indexing, and the row kernel's grid (128 rows x B*n_q*T / 32)
+  if (L > (int64_t{1} << 30) || B * n_kv * T > INT32_MAX || B * n_q * T > INT32_MAX / 4)
     return ATTN_ERR_UNSUPPORTED;
   if (workspace_bytes < attn_prefill_bwd_workspace_bytes(B, L, n_q, n_kv, d_h))
     return ATTN_ERR_INVALID_ARG;
@@ -837,7 +864,9 @@ attn_status_t attn_prefill_bwd(const void* q, const void* k, const void* v, cons
   p.status = status;
 
   const int64_t rows = B * n_q * T * kT;
-  rowdot_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+  constexpr int kRowdotRowsPerBlock = 8 * kRowdotRowsPerWarp;   // 256 threads
+  rowdot_kernel<<<static_cast<unsigned>((rows + kRowdotRowsPerBlock - 1) / kRowdotRowsPerBlock),
+                  256, 0, stream>>>(
       static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, nlse2, nrowdot,
       static_cast<int>(B), static_cast<int>(L), n_q, static_cast<int>(T * kT));
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
