@@ -56,8 +56,12 @@ class Dist:
         self.local_rank = _env_int("LOCAL_RANK", 0)
         self.pg = None
         if self.world > 1:
+            import datetime
             import torch.distributed as dist
-            dist.init_process_group("gloo")   # host-side barrier / max only
+            # host-side barrier / max only; BENCH_PG_TIMEOUT_S bounds how long a
+            # rank waits for a peer that never arrives
+            timeout = datetime.timedelta(seconds=_env_int("BENCH_PG_TIMEOUT_S", 1800))
+            dist.init_process_group("gloo", timeout=timeout)
             self.pg = dist
 
     def barrier(self):
