@@ -60,6 +60,15 @@ _SIGNATURES = {
                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                         ctypes.c_float, ctypes.c_void_p]),
     "attn_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p]),
+    "attn_prefill_host_staging_bytes": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int64,
+                                                         ctypes.c_int64, ctypes.c_int32,
+                                                         ctypes.c_int32, ctypes.c_int32]),
+    "attn_prefill_fwd_host": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                             ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
+                                             ctypes.c_void_p]),
     "attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_device_check": (ctypes.c_int, [ctypes.c_void_p]),
     "attn_prefill_grid_size": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,

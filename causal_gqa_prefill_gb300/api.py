@@ -211,6 +211,22 @@ def attn_device_check(stream=None) -> int:
     return int(_abi.load().attn_device_check(_stream_handle(stream)))
 
 
+def attn_prefill_host_staging_bytes(B, Lq, Lk, n_q, n_kv, d_h=128) -> int:
+    return int(_abi.load().attn_prefill_host_staging_bytes(int(B), int(Lq), int(Lk), int(n_q),
+                                                           int(n_kv), int(d_h)))
+
+
+def attn_prefill_fwd_host(q, k, v, o, lse, staging, staging_bytes, B, Lq, Lk, n_q, n_kv, d_h,
+                          causal, scale, stream=None) -> int:
+    """Direct call of the host-buffer C entry point (q, k, v, o, lse host
+    tensors or addresses; staging a device buffer); returns the raw status."""
+    lib = _abi.load()
+    return int(lib.attn_prefill_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                         _ptr(staging), int(staging_bytes), int(B), int(Lq),
+                                         int(Lk), int(n_q), int(n_kv), int(d_h), int(causal),
+                                         float(scale), _stream_handle(stream)))
+
+
 def attn_selftest_wait_timeout(spin_cycles: int, stream=None) -> int:
     """Enqueue the wait-limit diagnostic kernel (raw status of the launch)."""
     return int(_abi.load().attn_selftest_wait_timeout(int(spin_cycles), _stream_handle(stream)))

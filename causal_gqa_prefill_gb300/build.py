@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "lib")
 LIBNAME = "libattn_prefill.so"
-SOURCES = ["attn_prefill.cu", "attn_decode.cu", "attn_backward.cu"]
+SOURCES = ["attn_prefill.cu", "attn_decode.cu", "attn_backward.cu", "attn_host.cu"]
 HEADERS = [os.path.join(CSRC, "sm103_ptx.cuh"), os.path.join(INCLUDE, "attn_prefill.h")]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 

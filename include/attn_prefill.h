@@ -184,6 +184,36 @@ attn_status_t attn_prefill_bwd(const void* q, const void* k, const void* v, cons
                                int64_t B, int64_t L, int32_t n_q, int32_t n_kv, int32_t d_h,
                                int32_t causal, float scale, void* stream);
 
+/*
+ * Forward pass over host buffers (no counterpart on the pages: a deployment
+ * convenience for callers whose tensors live in host memory). Enqueues on
+ * `stream`: one cudaMemcpyAsync per input (q, k, v) into `staging`, the
+ * forward pass of attn_prefill_fwd_chunk there, and one cudaMemcpyAsync per
+ * result (o, lse) back to the host buffers. Returns after enqueueing; the
+ * host outputs are valid once the stream has reached that point.
+ *
+ *   q, k, v, o, lse  host pointers, same layouts and sizes as the device entry
+ *                    points (Lq = Lk is a square prefill). Page-locked host
+ *                    memory lets the copies overlap other work; pageable
+ *                    memory works but the copies may then synchronise.
+ *   staging          device memory of at least attn_prefill_host_staging_bytes
+ *                    bytes, 256-byte aligned, owned by the caller; holds the
+ *                    device copies of q, k, v, o, lse; contents on entry
+ *                    ignored, on exit unspecified. A call must not share a
+ *                    staging buffer with another call still in flight.
+ *   Returns ATTN_ERR_INVALID_ARG before enqueueing anything for NULL pointers,
+ *   a misaligned or too-small staging buffer and the argument errors of
+ *   attn_prefill_fwd_chunk; ATTN_ERR_UNSUPPORTED for its unsupported sizes;
+ *   ATTN_ERR_CUDA if a copy cannot be enqueued.
+ */
+int64_t attn_prefill_host_staging_bytes(int64_t B, int64_t Lq, int64_t Lk, int32_t n_q,
+                                        int32_t n_kv, int32_t d_h);  /* -1 on invalid sizes */
+attn_status_t attn_prefill_fwd_host(const void* q, const void* k, const void* v,
+                                    void* o, float* lse, void* staging, int64_t staging_bytes,
+                                    int64_t B, int64_t Lq, int64_t Lk, int32_t n_q,
+                                    int32_t n_kv, int32_t d_h, int32_t causal, float scale,
+                                    void* stream);
+
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* attn_status_string(attn_status_t status);
 

@@ -148,6 +148,28 @@ def test_backward_workspace_and_validation(lib):
     assert cg.attn_prefill_bwd(*bad, stream=0) == cg.ATTN_ERR_UNSUPPORTED
 
 
+def test_host_entry_staging_and_validation(lib):
+    need = cg.attn_prefill_host_staging_bytes(2, 300, 500, 8, 2, 128)
+    r = lambda x: (x + 255) // 256 * 256
+    q, kv, ls = 2 * 300 * 8 * 128 * 2, 2 * 500 * 2 * 128 * 2, 2 * 8 * 300 * 4
+    assert need == r(q) + 2 * r(kv) + r(q) + r(ls)
+    assert cg.attn_prefill_host_staging_bytes(2, 500, 300, 8, 2, 128) == -1     # Lk < Lq
+    assert cg.attn_prefill_host_staging_bytes(2, 300, 500, 8, 3, 128) == -1
+    assert cg.attn_prefill_host_staging_bytes(2, 300, 500, 8, 2, 96) == -1
+    args = [FAKE] * 6 + [need, 2, 300, 500, 8, 2, 128, 1, 0.1]
+    for idx in range(6):                                   # every pointer is required
+        bad = list(args); bad[idx] = 0
+        assert cg.attn_prefill_fwd_host(*bad, stream=0) == cg.ATTN_ERR_INVALID_ARG, idx
+    bad = list(args); bad[5] = FAKE + 128                  # staging not 256-byte aligned
+    assert cg.attn_prefill_fwd_host(*bad, stream=0) == cg.ATTN_ERR_INVALID_ARG
+    bad = list(args); bad[6] = need - 256                  # staging too small
+    assert cg.attn_prefill_fwd_host(*bad, stream=0) == cg.ATTN_ERR_INVALID_ARG
+    bad = list(args); bad[13] = 2                          # causal
+    assert cg.attn_prefill_fwd_host(*bad, stream=0) == cg.ATTN_ERR_INVALID_ARG
+    bad = list(args); bad[12] = 96                         # head dim
+    assert cg.attn_prefill_fwd_host(*bad, stream=0) == cg.ATTN_ERR_UNSUPPORTED
+
+
 def test_selftest_rejects_bad_limits(lib):
     assert cg.attn_selftest_wait_timeout(0, stream=0) == cg.ATTN_ERR_INVALID_ARG
     assert cg.attn_selftest_wait_timeout(-5, stream=0) == cg.ATTN_ERR_INVALID_ARG
