@@ -168,7 +168,7 @@ def attn_prefill_backward(q, k, v, o, lse, dout, *, causal=True, scale=None, wor
                           dq=None, dk=None, dv=None, stream=None):
     """Gradients (dq, dk, dv) of attn_prefill for the upstream gradient ``dout``.
 
-    q, o, dout: bf16 CUDA tensors [B, L, n_q, 128]; k, v: [B, L, n_kv, 128];
+    q, o, dout: bf16 CUDA tensors [B, L, n_q, d_h]; k, v: [B, L, n_kv, d_h], d_h 64 or 128;
     lse: the forward's fp32 [B, n_q, L]. Outputs are allocated unless passed
     in; ``workspace`` (at least attn_prefill_bwd_workspace_bytes bytes) is
     allocated with torch when not given."""

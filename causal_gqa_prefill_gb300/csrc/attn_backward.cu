@@ -51,9 +51,11 @@ namespace {
 
 using namespace gb300;
 
-constexpr int kD = 128;                  // head dimension
 constexpr int kT = 128;                  // rows per query tile and keys per key tile
-constexpr int kTileBytes = kT * kD * 2;  // one bf16 128 x 128 tile (two 64-column chunks)
+// One bf16 tile of 128 rows x D (D = 64 or 128 head dimensions): D / 64
+// chunks of 128 rows x 128 bytes, 128-byte swizzled.
+template <int D>
+__host__ __device__ constexpr int tile_bytes() { return kT * D * 2; }
 constexpr int kHalf = 64;                // score columns per half-step
 constexpr int kComputeWGs = 2;           // compute warpgroups
 constexpr int kCols = kHalf / kComputeWGs;   // dK/dV: half-step columns per warpgroup
@@ -153,6 +155,7 @@ __host__ __device__ constexpr uint32_t a_col(int kk) {
 // rows b_row0 .. b_row0 + 63 of a [128 rows x 128] K-major tile in shared memory.
 // The descriptor is built once; later K steps add their byte offset / 16 to
 // its start-address field (shared addresses stay below 2^18, so no carry).
+template <int D>
 __device__ __forceinline__ void mma_scores(bool leader, uint32_t d_tmem, uint32_t a_tmem,
                                            uint32_t b_smem, int b_row0) {
   constexpr uint32_t idesc = idesc_bf16_f32(kT, kHalf, false);
@@ -160,18 +163,19 @@ __device__ __forceinline__ void mma_scores(bool leader, uint32_t d_tmem, uint32_
   // issues tcgen05.mma faster than a lone lane in a divergent branch)
   const uint64_t b0 = sdesc_sw128(b_smem + b_row0 * 128, 16, 1024);
 #pragma unroll
-  for (int kk = 0; kk < kD / 16; ++kk) {
+  for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = (kk >> 2) * (kT * 128) + (kk & 3) * 32;
     if (leader) mma_ts(d_tmem, a_tmem + 8 * kk, b0 + (off >> 4), idesc, kk > 0 ? 1u : 0u);
   }
 }
 
-// This thread's row of a bf16 [B, L, H, 128] tensor into 64 TMEM columns of
+// This thread's row of a bf16 [B, L, H, D] tensor into D/2 TMEM columns of
 // its lane, as a tcgen05 A operand (column c = elements 2c, 2c+1, the lower in
 // the low half, which is the row's memory order); rows past L become zeros.
+template <int D>
 __device__ __forceinline__ void row_to_tmem(uint32_t taddr, const uint16_t* src, bool valid) {
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
+  for (int half = 0; half < D / 64; ++half) {
     uint32_t w[32];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
@@ -189,9 +193,10 @@ __device__ __forceinline__ void row_to_tmem(uint32_t taddr, const uint16_t* src,
 // D[128 x 128] (+)= A B over K = 64: A the bf16 P/dS of a half-step in TMEM
 // (a_col layout), B rows b_row0 .. b_row0 + 63 of a [128 rows x 128] tile,
 // used MN-major (its rows are the K dimension).
+template <int D>
 __device__ __forceinline__ void mma_accum(bool leader, uint32_t d_tmem, uint32_t a_tmem,
                                           uint32_t b_smem, int b_row0, bool accumulate) {
-  constexpr uint32_t idesc = idesc_bf16_f32(kT, kD, true);
+  constexpr uint32_t idesc = idesc_bf16_f32(kT, D, true);
   const uint64_t b0 = sdesc_sw128(b_smem + b_row0 * 128, kT * 128, 1024);
 #pragma unroll
   for (int kk = 0; kk < kHalf / 16; ++kk)
@@ -202,12 +207,13 @@ __device__ __forceinline__ void mma_accum(bool leader, uint32_t d_tmem, uint32_t
 
 // Scores of a whole tile: D[128 x 128] = A B^T over K = 128, A a fixed operand
 // in TMEM, B a [128 rows x 128] K-major tile in shared memory.
+template <int D>
 __device__ __forceinline__ void mma_scores_full(bool leader, uint32_t d_tmem, uint32_t a_tmem,
                                                 uint32_t b_smem) {
   constexpr uint32_t idesc = idesc_bf16_f32(kT, kT, false);
   const uint64_t b0 = sdesc_sw128(b_smem, 16, 1024);
 #pragma unroll
-  for (int kk = 0; kk < kD / 16; ++kk) {
+  for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = (kk >> 2) * (kT * 128) + (kk & 3) * 32;
     if (leader) mma_ts(d_tmem, a_tmem + 8 * kk, b0 + (off >> 4), idesc, kk > 0 ? 1u : 0u);
   }
@@ -215,9 +221,10 @@ __device__ __forceinline__ void mma_scores_full(bool leader, uint32_t d_tmem, ui
 
 // D[128 x 128] (+)= A B over K = 128: A the bf16 dS of a whole tile in TMEM
 // (a_col<kColsQ> layout), B a [128 rows x 128] tile used MN-major.
+template <int D>
 __device__ __forceinline__ void mma_accum_full(bool leader, uint32_t d_tmem, uint32_t a_tmem,
                                                uint32_t b_smem, bool accumulate) {
-  constexpr uint32_t idesc = idesc_bf16_f32(kT, kD, true);
+  constexpr uint32_t idesc = idesc_bf16_f32(kT, D, true);
   const uint64_t b0 = sdesc_sw128(b_smem, kT * 128, 1024);
 #pragma unroll
   for (int kk = 0; kk < kT / 16; ++kk)
@@ -290,6 +297,10 @@ __device__ __forceinline__ void store_chunk(uint32_t taddr, uint16_t* dst, float
 // 16-byte loads; a warp takes four rows so that its loads of all four are in
 // flight together. Rows past L get -inf and 0 without touching O or dO.
 constexpr int kRowdotRowsPerWarp = 4;
+__device__ __forceinline__ float dot2_bf16(uint32_t a, uint32_t d, float acc) {
+  acc = fmaf(__uint_as_float(a << 16), __uint_as_float(d << 16), acc);
+  return fmaf(__uint_as_float(a & 0xFFFF0000u), __uint_as_float(d & 0xFFFF0000u), acc);
+}
 __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 d) {
   float acc = __uint_as_float(a.x << 16) * __uint_as_float(d.x << 16);
   acc = fmaf(__uint_as_float(a.x & 0xFFFF0000u), __uint_as_float(d.x & 0xFFFF0000u), acc);
@@ -302,6 +313,9 @@ __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 d) {
   return acc;
 }
 
+// Lanes of a half-warp hold D / 16 dimensions each (8 for D = 128: one
+// 16-byte load; 4 for D = 64: the first half of it).
+template <int D>
 __global__ void rowdot_kernel(const uint16_t* o, const uint16_t* dout, const float* lse,
                               float* nlse2, float* nrowdot, int B, int L, int n_q, int Lp) {
   const int64_t total = static_cast<int64_t>(B) * n_q * Lp;
@@ -320,16 +334,25 @@ __global__ void rowdot_kernel(const uint16_t* o, const uint16_t* dout, const flo
       if (t < L) {
         const int h = static_cast<int>(bh % n_q);
         const int b = static_cast<int>(bh / n_q);
-        const size_t off = ((static_cast<size_t>(b) * L + t) * n_q + h) * kD + 8 * l16;
-        a[k] = *reinterpret_cast<const uint4*>(o + off);
-        d[k] = *reinterpret_cast<const uint4*>(dout + off);
+        const size_t off = ((static_cast<size_t>(b) * L + t) * n_q + h) * D + (D / 16) * l16;
+        if (D == 128) {
+          a[k] = *reinterpret_cast<const uint4*>(o + off);
+          d[k] = *reinterpret_cast<const uint4*>(dout + off);
+        } else {
+          const uint2 a2 = *reinterpret_cast<const uint2*>(o + off);
+          const uint2 d2 = *reinterpret_cast<const uint2*>(dout + off);
+          a[k] = make_uint4(a2.x, a2.y, 0u, 0u);
+          d[k] = make_uint4(d2.x, d2.y, 0u, 0u);
+        }
         live[k] = true;
       }
     }
   }
 #pragma unroll
   for (int k = 0; k < kRowdotRowsPerWarp / 2; ++k) {
-    float dd = live[k] ? dot8_bf16(a[k], d[k]) : 0.0f;
+    float dd = 0.0f;
+    if (live[k]) dd = (D == 128) ? dot8_bf16(a[k], d[k])
+                                 : dot2_bf16(a[k].y, d[k].y, dot2_bf16(a[k].x, d[k].x, 0.0f));
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, off);
     const int64_t row = warp_id * kRowdotRowsPerWarp + 2 * k + half;
@@ -355,18 +378,20 @@ __device__ __forceinline__ void drain_ring(Sync& sy, int issued) {
 
 // SS product for dP^T of a half-step: D[128 x 64] = V_j dO^T over K = 128 (d),
 // both operands K-major tiles in shared memory (B rows b_row0 .. b_row0 + 63).
+template <int D>
 __device__ __forceinline__ void mma_scores_ss(bool leader, uint32_t d_tmem, uint32_t a_smem,
                                               uint32_t b_smem, int b_row0) {
   constexpr uint32_t idesc = idesc_bf16_f32(kT, kHalf, false);
   const uint64_t a0 = sdesc_sw128(a_smem, 16, 1024);
   const uint64_t b0 = sdesc_sw128(b_smem + b_row0 * 128, 16, 1024);
 #pragma unroll
-  for (int kk = 0; kk < kD / 16; ++kk) {
+  for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = ((kk >> 2) * (kT * 128) + (kk & 3) * 32) >> 4;
     if (leader) mma_ss(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
             const __grid_constant__ CUtensorMap tmV, const uint16_t* __restrict__ k_rows,
@@ -374,6 +399,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Sync sy;
   // smem: V_j | kStagesKV x [Q_i | dO_i | -LSE*log2 e [128] | -D [128]]
+  constexpr int kTileBytes = tile_bytes<D>();
   const uint32_t base = (smem_addr(dyn_smem) + 1023u) & ~1023u;
   const uint32_t sV = base, sRing = base + kTileBytes;
   constexpr uint32_t kStage = 2 * kTileBytes + 1024;
@@ -387,17 +413,17 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   const int nhalf = 2 * nsteps;                        // half-steps of 64 queries
   setup(sy);
   const uint32_t tmem = sy.tmem_base;
-  // TMEM columns: K_j 0..63 (A operand), S^T of half-step u in buffer u&1 at
-  // 64 + 64*(u&1) (P^T is written over it), dP^T 192..255 (dS^T over it),
-  // dV 256..383, dK 384..511. With two S^T buffers the tensor cores compute
-  // S^T(u+1) while the compute warps are still on half-step u.
-  constexpr uint32_t cK = 0, cS = 64, cP = 192, cDV = 256, cDK = 384;
+  // TMEM columns: K_j 0..D/2-1 (A operand), S^T of half-step u in buffer
+  // u&1 at 64 + 64*(u&1) (P^T is written over it), dP^T 192..255 (dS^T over
+  // it), dV at 256 and dK at 256 + D (D columns each). With two S^T buffers
+  // the tensor cores compute S^T(u+1) while the compute warps are still on u.
+  constexpr uint32_t cK = 0, cS = 64, cP = 192, cDV = 256, cDK = 256 + D;
 
   if (warp == kLoadWarp) {
     if (lane == 0) {
       const uint32_t fb = smem_addr(&sy.fixed_full);
       mbar_arrive_expect_tx(fb, kTileBytes);
-      for (int c = 0; c < 2; ++c) tma_load_4d(sV + c * kT * 128, &tmV, fb, c * 64, kvh, j * kT, b);
+      for (int c = 0; c < D / 64; ++c) tma_load_4d(sV + c * kT * 128, &tmV, fb, c * 64, kvh, j * kT, b);
       int t = 0;
       for (; t < nsteps; ++t) {
         const int st = t % kStagesKV, use = t / kStagesKV;
@@ -406,7 +432,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         const int i = i0 + t % (p.T - i0);
         const uint32_t dst = sRing + st * kStage, bar = smem_addr(&sy.full[st]);
         mbar_arrive_expect_tx(bar, 2 * kTileBytes + 1024);
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           tma_load_4d(dst + c * kT * 128, &tmQ, bar, c * 64, h, i * kT, b);
           tma_load_4d(dst + kTileBytes + c * kT * 128, &tmdO, bar, c * 64, h, i * kT, b);
         }
@@ -433,11 +459,11 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       return true;
     };
     auto issue_st = [&](int u) {      // S^T(u) = K Q^T into buffer u&1
-      mma_scores(leader, tmem + cS + 64 * (u & 1), tmem + cK, stage_of(u), 64 * (u & 1));
+      mma_scores<D>(leader, tmem + cS + 64 * (u & 1), tmem + cK, stage_of(u), 64 * (u & 1));
       if (leader) mma_commit(smem_addr(&sy.s_full[u & 1]));
     };
     auto issue_dpt = [&](int u) {     // dP^T(u) = V dO^T
-      mma_scores_ss(leader, tmem + cP, sV, stage_of(u) + kTileBytes, 64 * (u & 1));
+      mma_scores_ss<D>(leader, tmem + cP, sV, stage_of(u) + kTileBytes, 64 * (u & 1));
       if (leader) mma_commit(smem_addr(&sy.dp_full));
     };
     if (ok && (ok = wait_stage(0))) {
@@ -460,10 +486,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                       wait_bounded(smem_addr(&sy.p_full[u & 1]), (u >> 1) & 1, sy, p)))
         break;
       tc_fence_after_sync();
-      mma_accum(leader, tmem + cDV, tmem + cS + 64 * (u & 1), sdO, r0, u > 0);   // dV += P^T dO
+      mma_accum<D>(leader, tmem + cDV, tmem + cS + 64 * (u & 1), sdO, r0, u > 0);   // dV += P^T dO
       if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.ds_full), u & 1, sy, p))) break;
       tc_fence_after_sync();
-      mma_accum(leader, tmem + cDK, tmem + cP, sQ, r0, u > 0);                   // dK += dS^T Q
+      mma_accum<D>(leader, tmem + cDK, tmem + cP, sQ, r0, u > 0);                   // dK += dS^T Q
       if (leader && (u & 1)) mma_commit(smem_addr(&sy.empty[(u >> 1) % kStagesKV]));
       if (more) issue_dpt(u + 1);
     }
@@ -478,8 +504,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     const int krow = j * kT + r;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     // K_j becomes the A operand of S^T in TMEM (first warpgroup)
-    const size_t koff = ((static_cast<size_t>(b) * p.L + krow) * p.n_kv + kvh) * kD;
-    if (cw == 0) row_to_tmem(lane_base + cK, k_rows + koff, krow < p.L);
+    const size_t koff = ((static_cast<size_t>(b) * p.L + krow) * p.n_kv + kvh) * D;
+    if (cw == 0) row_to_tmem<D>(lane_base + cK, k_rows + koff, krow < p.L);
     tmem_wait_st();
     tc_fence_before_sync();
     mbar_arrive(smem_addr(&sy.a_ready));
@@ -569,11 +595,12 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     if (ok && __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.done), 0, sy, p))) {
       tc_fence_after_sync();
       const bool valid = krow < p.L;
-      // 8 chunks of 32 columns (dV then dK) shared out over the warpgroups
+      // 2*D/32 chunks of 32 columns (dV then dK) shared out over the warpgroups
+      constexpr int kOut = 2 * D / 32, kPer = kOut / kComputeWGs, kHalfOut = D / 32;
 #pragma unroll 1
-      for (int q = cw * (8 / kComputeWGs); q < (cw + 1) * (8 / kComputeWGs); ++q) {
-        const int col = (q & 3) * 32;
-        if (q < 4) store_chunk(lane_base + cDV + col, p.dv + koff + col, 1.0f, valid);
+      for (int q = cw * kPer; q < (cw + 1) * kPer; ++q) {
+        const int col = (q % kHalfOut) * 32;
+        if (q < kHalfOut) store_chunk(lane_base + cDV + col, p.dv + koff + col, 1.0f, valid);
         else store_chunk(lane_base + cDK + col, p.dk + koff + col, p.scale, valid);
       }
     }
@@ -583,6 +610,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
 
 // ------------------------------------------------------------------------ dQ
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
           const uint16_t* __restrict__ q_rows, const uint16_t* __restrict__ do_rows,
@@ -590,6 +618,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Sync sy;
   // smem: kStages x [K_t | V_t]
+  constexpr int kTileBytes = tile_bytes<D>();
   const uint32_t base = (smem_addr(dyn_smem) + 1023u) & ~1023u;
   constexpr uint32_t kStage = 2 * kTileBytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -601,7 +630,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
   const int n = p.causal ? i + 1 : p.T;                // key tiles
   setup(sy);
   const uint32_t tmem = sy.tmem_base;
-  // TMEM columns: Q_i 0..63 and dO_i 64..127 (A operands), S 128..255,
+  // TMEM columns: Q_i at 0 and dO_i at 64 (D/2 columns each, A operands), S 128..255,
   // dP 256..383 (dS is written over it), dQ 384..511. Per key tile t the
   // tensor cores run S(t+1) while the compute warps finish dS(t), and dQ(t)
   // plus dP(t+1) while they turn S(t+1) into P(t+1).
@@ -615,7 +644,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
         if (use > 0 && !wait_bounded(smem_addr(&sy.empty[st]), (use - 1) & 1, sy, p)) break;
         const uint32_t dst = base + st * kStage, bar = smem_addr(&sy.full[st]);
         mbar_arrive_expect_tx(bar, 2 * kTileBytes);
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           tma_load_4d(dst + c * kT * 128, &tmK, bar, c * 64, kvh, t * kT, b);
           tma_load_4d(dst + kTileBytes + c * kT * 128, &tmV, bar, c * 64, kvh, t * kT, b);
         }
@@ -635,9 +664,9 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
       return true;
     };
     if (ok && (ok = wait_stage(0))) {
-      mma_scores_full(leader, tmem + cS, tmem + cQ, stage_of(0));               // S  = Q K^T
+      mma_scores_full<D>(leader, tmem + cS, tmem + cQ, stage_of(0));               // S  = Q K^T
       if (leader) mma_commit(smem_addr(&sy.s_full[0]));
-      mma_scores_full(leader, tmem + cP, tmem + cO, stage_of(0) + kTileBytes);  // dP = dO V^T
+      mma_scores_full<D>(leader, tmem + cP, tmem + cO, stage_of(0) + kTileBytes);  // dP = dO V^T
       if (leader) mma_commit(smem_addr(&sy.dp_full));
     }
     for (int t = 0; t < n && ok; ++t) {
@@ -646,15 +675,15 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
       if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.p_full[0]), t & 1, sy, p))) break;
       if (more) {
         if (!wait_stage(t + 1)) break;
-        mma_scores_full(leader, tmem + cS, tmem + cQ, stage_of(t + 1));
+        mma_scores_full<D>(leader, tmem + cS, tmem + cQ, stage_of(t + 1));
         if (leader) mma_commit(smem_addr(&sy.s_full[0]));
       }
       if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.ds_full), t & 1, sy, p))) break;
       tc_fence_after_sync();
-      mma_accum_full(leader, tmem + cDQ, tmem + cP, stage_of(t), t > 0);        // dQ += dS K
+      mma_accum_full<D>(leader, tmem + cDQ, tmem + cP, stage_of(t), t > 0);        // dQ += dS K
       if (leader) mma_commit(smem_addr(&sy.empty[t % kStages]));
       if (more) {
-        mma_scores_full(leader, tmem + cP, tmem + cO, stage_of(t + 1) + kTileBytes);
+        mma_scores_full<D>(leader, tmem + cP, tmem + cO, stage_of(t + 1) + kTileBytes);
         if (leader) mma_commit(smem_addr(&sy.dp_full));
       }
     }
@@ -668,9 +697,9 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
     const int r = (warp & 3) * 32 + lane;
     const int row = i * kT + r;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const size_t qoff = ((static_cast<size_t>(b) * p.L + row) * p.n_q + h) * kD;
+    const size_t qoff = ((static_cast<size_t>(b) * p.L + row) * p.n_q + h) * D;
     // Q_i (first warpgroup) and dO_i (second) become the A operands in TMEM
-    if (cw < 2) row_to_tmem(lane_base + (cw ? cO : cQ), (cw ? do_rows : q_rows) + qoff, row < p.L);
+    if (cw < 2) row_to_tmem<D>(lane_base + (cw ? cO : cQ), (cw ? do_rows : q_rows) + qoff, row < p.L);
     tmem_wait_st();
     tc_fence_before_sync();
     mbar_arrive(smem_addr(&sy.a_ready));
@@ -740,8 +769,9 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
     }
     if (ok && __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.done), 0, sy, p))) {
       tc_fence_after_sync();
+      constexpr int kPer = (D / 32) / kComputeWGs;    // chunks of 32 dQ columns per warpgroup
 #pragma unroll 1
-      for (int q = cw * (4 / kComputeWGs); q < (cw + 1) * (4 / kComputeWGs); ++q)
+      for (int q = cw * kPer; q < (cw + 1) * kPer; ++q)
         store_chunk(lane_base + cDQ + 32 * q, p.dq + qoff + 32 * q, p.scale, row < p.L);
     }
   }
@@ -758,8 +788,10 @@ constexpr int kMaxDevices = 64;
 std::mutex g_bwd_mutex;
 bool g_bwd_ready[kMaxDevices];
 EncodeTiledFn g_bwd_encode = nullptr;
-constexpr int kDkdvSmem = kTileBytes + kStagesKV * (2 * kTileBytes + 1024) + 1024;
-constexpr int kDqSmem = kStages * (2 * kTileBytes) + 1024;
+template <int D>
+constexpr int dkdv_smem() { return tile_bytes<D>() + kStagesKV * (2 * tile_bytes<D>() + 1024) + 1024; }
+template <int D>
+constexpr int dq_smem() { return kStages * (2 * tile_bytes<D>()) + 1024; }
 
 attn_status_t bwd_device_ready(cudaStream_t stream, int** status) {
   int dev = 0;
@@ -779,21 +811,26 @@ attn_status_t bwd_device_ready(cudaStream_t stream, int** status) {
         return ATTN_ERR_CUDA;
       g_bwd_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
-    if (cudaFuncSetAttribute(dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kDkdvSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDqSmem) !=
-            cudaSuccess)
+    if (cudaFuncSetAttribute(dkdv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dkdv_smem<128>()) != cudaSuccess ||
+        cudaFuncSetAttribute(dq_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dq_smem<128>()) != cudaSuccess ||
+        cudaFuncSetAttribute(dkdv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dkdv_smem<64>()) != cudaSuccess ||
+        cudaFuncSetAttribute(dq_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dq_smem<64>()) != cudaSuccess)
       return ATTN_ERR_CUDA;
     g_bwd_ready[dev] = true;
   }
   return ATTN_OK;
 }
 
-bool encode_tile_map(CUtensorMap* map, const void* ptr, int H, int64_t L, int64_t B) {
-  const cuuint64_t dims[4] = {kD, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(L),
+bool encode_tile_map(CUtensorMap* map, const void* ptr, int D, int H, int64_t L, int64_t B) {
+  const cuuint64_t d = static_cast<cuuint64_t>(D);
+  const cuuint64_t dims[4] = {d, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(L),
                               static_cast<cuuint64_t>(B)};
-  const cuuint64_t strides[3] = {kD * 2, static_cast<cuuint64_t>(H) * kD * 2,
-                                 static_cast<cuuint64_t>(L) * H * kD * 2};
+  const cuuint64_t strides[3] = {d * 2, static_cast<cuuint64_t>(H) * d * 2,
+                                 static_cast<cuuint64_t>(L) * H * d * 2};
   const cuuint32_t box[4] = {64, 1, kT, 1};
   const cuuint32_t estride[4] = {1, 1, 1, 1};
   return g_bwd_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims,
@@ -808,7 +845,7 @@ extern "C" {
 
 int64_t attn_prefill_bwd_workspace_bytes(int64_t B, int64_t L, int32_t n_q, int32_t n_kv,
                                          int32_t d_h) {
-  if (B < 1 || L < 1 || n_q < 1 || n_kv < 1 || n_q % n_kv != 0 || d_h != kD) return -1;
+  if (B < 1 || L < 1 || n_q < 1 || n_kv < 1 || n_q % n_kv != 0 || (d_h != 64 && d_h != 128)) return -1;
   const int64_t T = (L + kT - 1) / kT;
   return 2 * B * n_q * T * kT * 4;
 }
@@ -829,7 +866,7 @@ attn_status_t attn_prefill_bwd(const void* q, const void* k, const void* v, cons
       misaligned(dout, 16) || misaligned(dq, 16) || misaligned(dk, 16) || misaligned(dv, 16) ||
       misaligned(lse, 4) || misaligned(workspace, 16))
     return ATTN_ERR_INVALID_ARG;
-  if (d_h != kD) return ATTN_ERR_UNSUPPORTED;
+  if (d_h != 64 && d_h != 128) return ATTN_ERR_UNSUPPORTED;
   const int64_t T = (L + kT - 1) / kT;
   // 32-bit tile indexing, and the row kernel's grid (128 rows x B*n_q*T / 32)
   if (L > (int64_t{1} << 30) || B * n_kv * T > INT32_MAX || B * n_q * T > INT32_MAX / 4)
@@ -842,8 +879,8 @@ attn_status_t attn_prefill_bwd(const void* q, const void* k, const void* v, cons
   if (ds != ATTN_OK) return ds;
 
   CUtensorMap mq, mk, mv, mdo;
-  if (!encode_tile_map(&mq, q, n_q, L, B) || !encode_tile_map(&mk, k, n_kv, L, B) ||
-      !encode_tile_map(&mv, v, n_kv, L, B) || !encode_tile_map(&mdo, dout, n_q, L, B))
+  if (!encode_tile_map(&mq, q, d_h, n_q, L, B) || !encode_tile_map(&mk, k, d_h, n_kv, L, B) ||
+      !encode_tile_map(&mv, v, d_h, n_kv, L, B) || !encode_tile_map(&mdo, dout, d_h, n_q, L, B))
     return ATTN_ERR_CUDA;
   BwdParams p;
   p.L = static_cast<int>(L);
@@ -865,18 +902,30 @@ attn_status_t attn_prefill_bwd(const void* q, const void* k, const void* v, cons
 
   const int64_t rows = B * n_q * T * kT;
   constexpr int kRowdotRowsPerBlock = 8 * kRowdotRowsPerWarp;   // 256 threads
-  rowdot_kernel<<<static_cast<unsigned>((rows + kRowdotRowsPerBlock - 1) / kRowdotRowsPerBlock),
-                  256, 0, stream>>>(
-      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, nlse2, nrowdot,
-      static_cast<int>(B), static_cast<int>(L), n_q, static_cast<int>(T * kT));
-  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  const unsigned row_blocks =
+      static_cast<unsigned>((rows + kRowdotRowsPerBlock - 1) / kRowdotRowsPerBlock);
+  const uint16_t* oh = static_cast<const uint16_t*>(o);
   const uint16_t* qh = static_cast<const uint16_t*>(q);
   const uint16_t* kh = static_cast<const uint16_t*>(k);
   const uint16_t* doh = static_cast<const uint16_t*>(dout);
-  dkdv_kernel<<<static_cast<unsigned>(B * n_kv * T), kThreads, kDkdvSmem, stream>>>(mq, mdo, mv,
-                                                                                     kh, p);
-  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-  dq_kernel<<<static_cast<unsigned>(B * n_q * T), kThreads, kDqSmem, stream>>>(mk, mv, qh, doh, p);
+  const int Lp = static_cast<int>(T * kT);
+  const unsigned kv_tiles = static_cast<unsigned>(B * n_kv * T);
+  const unsigned q_tiles = static_cast<unsigned>(B * n_q * T);
+  if (d_h == 128) {
+    rowdot_kernel<128><<<row_blocks, 256, 0, stream>>>(oh, doh, lse, nlse2, nrowdot,
+                                                       static_cast<int>(B), p.L, n_q, Lp);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    dkdv_kernel<128><<<kv_tiles, kThreads, dkdv_smem<128>(), stream>>>(mq, mdo, mv, kh, p);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    dq_kernel<128><<<q_tiles, kThreads, dq_smem<128>(), stream>>>(mk, mv, qh, doh, p);
+  } else {
+    rowdot_kernel<64><<<row_blocks, 256, 0, stream>>>(oh, doh, lse, nlse2, nrowdot,
+                                                      static_cast<int>(B), p.L, n_q, Lp);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    dkdv_kernel<64><<<kv_tiles, kThreads, dkdv_smem<64>(), stream>>>(mq, mdo, mv, kh, p);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    dq_kernel<64><<<q_tiles, kThreads, dq_smem<64>(), stream>>>(mk, mv, qh, doh, p);
+  }
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

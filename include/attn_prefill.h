@@ -172,7 +172,7 @@ attn_status_t attn_decode_fwd(const void* q, const void* k, const void* v, void*
  *   workspace         device memory of at least attn_prefill_bwd_workspace_bytes
  *                     bytes, 16-byte aligned, owned by the caller; contents on
  *                     entry ignored, on exit unspecified
- *   d_h must be 128 (ATTN_ERR_UNSUPPORTED otherwise); square problems only
+ *   d_h must be 64 or 128 (ATTN_ERR_UNSUPPORTED otherwise); square problems only
  *   (the forward's Lq = Lk = L). Everything else as attn_prefill_fwd.
  */
 int64_t attn_prefill_bwd_workspace_bytes(int64_t B, int64_t L, int32_t n_q, int32_t n_kv,

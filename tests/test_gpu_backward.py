@@ -64,8 +64,8 @@ def run_backward(q, k, v, dout, causal=True, scale=None):
     return dq, dk, dv
 
 
-def inputs(B, L, n_q, n_kv, causal=True, number=0):
-    w = W.custom(B, L, n_q, n_kv, 128, causal=causal, number=number, backward=True)
+def inputs(B, L, n_q, n_kv, causal=True, number=0, d_h=128):
+    w = W.custom(B, L, n_q, n_kv, d_h, causal=causal, number=number, backward=True)
     q, k, v = W.make_inputs(w)
     return w, q, k, v, W.make_grad(w)
 
@@ -129,12 +129,34 @@ def test_backward_deterministic():
         assert torch.equal(x, y)
 
 
-def test_backward_head_dim_64_unsupported():
-    w = W.custom(1, 128, 2, 1, 64)
-    q, k, v = W.make_inputs(w)
-    o, lse = attn_prefill(q, k, v)
+SHAPES_D64 = [
+    # B, L, n_q, n_kv, causal; head dimension 64 (one 128-byte swizzle chunk per row)
+    (1, 256, 4, 1, True),        # the tiny GQA-4 layer (L = 256, d_h = 64)
+    (2, 300, 4, 2, True),        # batch, ragged tail
+    (1, 130, 3, 3, False),       # full attention, MHA, two-row tail
+    (1, 700, 8, 1, True),        # GQA-8, several tiles
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES_D64,
+                         ids=[f"d64-B{s[0]}L{s[1]}h{s[2]}-{s[3]}{'c' if s[4] else 'f'}"
+                              for s in SHAPES_D64])
+def test_backward_head_dim_64(shape):
+    B, L, n_q, n_kv, causal = shape
+    w, q, k, v, dout = inputs(B, L, n_q, n_kv, causal, number=1400 + L, d_h=64)
+    gpu = run_backward(q, k, v, dout, causal=causal)
+    ref = oracle.attention_backward(to_np(q), to_np(k), to_np(v), to_np(dout), causal=causal)
+    errs = assert_grads(gpu, ref, str(shape))
+    print(shape, errs)
+
+
+def test_backward_head_dim_32_unsupported():
+    q = torch.zeros(1, 128, 2, 32, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(1, 128, 1, 32, dtype=torch.bfloat16, device="cuda")
+    o = torch.zeros_like(q)
+    lse = torch.zeros(1, 2, 128, dtype=torch.float32, device="cuda")
     with pytest.raises(AttnError) as e:
-        attn_prefill_backward(q, k, v, o, lse, torch.randn_like(q))
+        attn_prefill_backward(q, k, k, o, lse, torch.zeros_like(q))
     assert e.value.status == ATTN_ERR_UNSUPPORTED
 
 
