@@ -139,7 +139,7 @@ attn_status_t attn_prefill_fwd_fp8(const void* q, const void* k, const void* v,
  *   workspace  device memory of at least attn_decode_workspace_bytes(...)
  *              bytes, 16-byte aligned, owned by the caller; its contents
  *              on entry are ignored and on exit unspecified.
- *   n_q / n_kv <= 8 and d_h = 128 (ATTN_ERR_UNSUPPORTED otherwise); a NULL
+ *   n_q / n_kv <= 16 and d_h = 128 (ATTN_ERR_UNSUPPORTED otherwise); a NULL
  *   or too-small workspace is ATTN_ERR_INVALID_ARG. Everything else as
  *   attn_prefill_fwd.
  */

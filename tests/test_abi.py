@@ -120,14 +120,17 @@ def test_decode_workspace_and_validation(lib):
     assert cg.attn_decode_fwd(*bad, stream=0) == cg.ATTN_ERR_INVALID_ARG
     bad = list(args); bad[11] = 64                     # head dim
     assert cg.attn_decode_fwd(*bad, stream=0) == cg.ATTN_ERR_UNSUPPORTED
-    bad = list(args); bad[9], bad[10] = 18, 2          # g = 9
+    bad = list(args); bad[9], bad[10] = 34, 2          # g = 17
     assert cg.attn_decode_fwd(*bad, stream=0) == cg.ATTN_ERR_UNSUPPORTED
+    assert cg.attn_decode_workspace_bytes(1, 1000, 32, 2) > 0     # g = 16
+    assert cg.attn_decode_workspace_bytes(1, 1000, 34, 2) == -1   # g = 17
 
 
 def test_backward_workspace_and_validation(lib):
     need = cg.attn_prefill_bwd_workspace_bytes(2, 300, 8, 2)
     assert need == 2 * 2 * 8 * 384 * 4        # LSE*log2(e) and D, padded to 128-row tiles
-    assert cg.attn_prefill_bwd_workspace_bytes(2, 300, 8, 2, 64) == -1
+    assert cg.attn_prefill_bwd_workspace_bytes(2, 300, 8, 2, 64) == need   # independent of d_h
+    assert cg.attn_prefill_bwd_workspace_bytes(2, 300, 8, 2, 32) == -1
     assert cg.attn_prefill_bwd_workspace_bytes(2, 300, 8, 3) == -1
     assert cg.attn_prefill_bwd_workspace_bytes(0, 300, 8, 2) == -1
     args = [FAKE] * 10 + [need, 2, 300, 8, 2, 128, 1, 0.1]
@@ -144,7 +147,7 @@ def test_backward_workspace_and_validation(lib):
     assert cg.attn_prefill_bwd(*bad, stream=0) == cg.ATTN_ERR_INVALID_ARG
     bad = list(args); bad[14] = 3                        # n_q % n_kv
     assert cg.attn_prefill_bwd(*bad, stream=0) == cg.ATTN_ERR_INVALID_ARG
-    bad = list(args); bad[15] = 64                       # head dim
+    bad = list(args); bad[15] = 96                       # head dim
     assert cg.attn_prefill_bwd(*bad, stream=0) == cg.ATTN_ERR_UNSUPPORTED
 
 

@@ -37,7 +37,12 @@ DECODE = [
     (4, 777, 4, 4),        # g = 1
     (1, 2049, 8, 1),       # g = 8, ragged last tile
     (1, 5000, 32, 8),
-    (2, 64, 2, 2),         # exactly one tile
+    (2, 64, 2, 2),         # a partial first tile only
+    (1, 128, 4, 1),        # exactly one whole tile
+    (3, 700, 10, 5),       # 90 tiles: fewer tiles than CTAs, one tile per CTA
+    (2, 20000, 6, 3),      # 942 tiles over 152 CTAs: ranges cross head boundaries
+    (1, 3000, 12, 1),      # g = 12
+    (2, 1500, 32, 2),      # g = 16
 ]
 
 
@@ -80,13 +85,13 @@ def test_decode_workloads(num):
 
 
 def test_decode_argument_errors():
-    q = torch.zeros(1, 1, 16, 128, device="cuda", dtype=torch.bfloat16)
+    q = torch.zeros(1, 1, 17, 128, device="cuda", dtype=torch.bfloat16)
     kv = torch.zeros(1, 64, 1, 128, device="cuda", dtype=torch.bfloat16)
     o = torch.empty_like(q)
-    lse = torch.empty(1, 16, 1, device="cuda")
+    lse = torch.empty(1, 17, 1, device="cuda")
     ws = torch.empty(1 << 16, dtype=torch.uint8, device="cuda")
-    assert attn_decode_fwd(q, kv, kv, o, lse, ws, ws.numel(), 1, 64, 16, 1, 128, 0.1) == \
-        ATTN_ERR_UNSUPPORTED                                  # g = 16 > 8
+    assert attn_decode_fwd(q, kv, kv, o, lse, ws, ws.numel(), 1, 64, 17, 1, 128, 0.1) == \
+        ATTN_ERR_UNSUPPORTED                                  # g = 17 > 16
     q = torch.zeros(1, 1, 8, 128, device="cuda", dtype=torch.bfloat16)
     need = attn_decode_workspace_bytes(1, 64, 8, 1)
     assert attn_decode_fwd(q, kv, kv, torch.empty_like(q), lse, ws, need - 1, 1, 64, 8, 1, 128,
