@@ -89,7 +89,8 @@ struct Sync {
   uint64_t fixed_full;              // dK/dV: V_j has landed in shared memory
   uint64_t full[kStages], empty[kStages];
   uint64_t s_full[2], p_full[2];    // scores ready (commit) / P or dS ready (compute threads)
-  uint64_t dp_full, ds_full;        // dkdv: dP^T ready (commit) / dS^T ready (compute threads)
+  uint64_t dp_full, ds_full;        // dP (dP^T) ready (commit) / dS (dS^T) ready (compute threads)
+  uint64_t dp_free, dq_done;        // dQ: dP read out (compute threads) / dQ += dS K done (commit)
   uint64_t done, drain;
   uint32_t tmem_base;
   int abort;
@@ -233,6 +234,35 @@ __device__ __forceinline__ void mma_accum_full(bool leader, uint32_t d_tmem, uin
              (accumulate || kk > 0) ? 1u : 0u);
 }
 
+// dQ[128 x D] (+)= dS K over K = 128 keys: dS bf16 in TMEM, packed two keys
+// per column (K step kk at column 8*kk), K a [128 keys x D] tile used MN-major.
+template <int D>
+__device__ __forceinline__ void mma_accum_dq(bool leader, uint32_t d_tmem, uint32_t a_tmem,
+                                             uint32_t b_smem, bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kT, D, true);
+  const uint64_t b0 = sdesc_sw128(b_smem, kT * 128, 1024);
+#pragma unroll
+  for (int kk = 0; kk < kT / 16; ++kk)
+    if (leader)
+      mma_ts(d_tmem, a_tmem + 8 * kk, b0 + ((kk * 16 * 128) >> 4), idesc,
+             (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// D[128 x 128] = A B^T over K = D: A a [128 rows x D] K-major tile in shared
+// memory (dO), B a [128 rows x D] K-major tile (V).
+template <int D>
+__device__ __forceinline__ void mma_scores_full_ss(bool leader, uint32_t d_tmem, uint32_t a_smem,
+                                                   uint32_t b_smem) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kT, kT, false);
+  const uint64_t a0 = sdesc_sw128(a_smem, 16, 1024);
+  const uint64_t b0 = sdesc_sw128(b_smem, 16, 1024);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = ((kk >> 2) * (kT * 128) + (kk & 3) * 32) >> 4;
+    if (leader) mma_ss(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
 __device__ __forceinline__ void setup(Sync& sy) {
   if (threadIdx.x == 0) {
     mbar_init(smem_addr(&sy.a_ready), kComputeThreads);
@@ -247,6 +277,8 @@ __device__ __forceinline__ void setup(Sync& sy) {
     }
     mbar_init(smem_addr(&sy.dp_full), 1);
     mbar_init(smem_addr(&sy.ds_full), kComputeThreads);
+    mbar_init(smem_addr(&sy.dp_free), kComputeThreads);
+    mbar_init(smem_addr(&sy.dq_done), 1);
     mbar_init(smem_addr(&sy.done), 1);
     mbar_init(smem_addr(&sy.drain), 1);
     sy.abort = 0;
@@ -613,13 +645,14 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-          const uint16_t* __restrict__ q_rows, const uint16_t* __restrict__ do_rows,
+          const __grid_constant__ CUtensorMap tmdO, const uint16_t* __restrict__ q_rows,
           const BwdParams p) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Sync sy;
-  // smem: kStages x [K_t | V_t]
+  // smem: dO_i | kStages x [K_t | V_t]
   constexpr int kTileBytes = tile_bytes<D>();
   const uint32_t base = (smem_addr(dyn_smem) + 1023u) & ~1023u;
+  const uint32_t sdO = base, sRing = base + kTileBytes;
   constexpr uint32_t kStage = 2 * kTileBytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int groups = static_cast<int>(gridDim.x) / p.T;   // B * n_q
@@ -630,32 +663,38 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
   const int n = p.causal ? i + 1 : p.T;                // key tiles
   setup(sy);
   const uint32_t tmem = sy.tmem_base;
-  // TMEM columns: Q_i at 0 and dO_i at 64 (D/2 columns each, A operands), S 128..255,
-  // dP 256..383 (dS is written over it), dQ 384..511. Per key tile t the
-  // tensor cores run S(t+1) while the compute warps finish dS(t), and dQ(t)
-  // plus dP(t+1) while they turn S(t+1) into P(t+1).
-  constexpr uint32_t cQ = 0, cO = 64, cS = 128, cP = 256, cDQ = 384;
+  // TMEM columns: Q_i at 0 (D/2 columns, the A operand of S), S 64..191,
+  // dP 192..319, dS 320..383 (bf16, two keys per column), dQ 384..511.
+  // dP is read out before dS is formed and dS has its own columns, so per key
+  // tile t the tensor cores run S(t+1) and dP(t+1) while the compute warps
+  // still work on tile t, and dQ(t) as soon as dS(t) is in.
+  constexpr uint32_t cQ = 0, cS = 64, cP = 192, cDS = 320, cDQ = 384;
 
   if (warp == kLoadWarp) {
     if (lane == 0) {
+      const uint32_t fb = smem_addr(&sy.fixed_full);
+      mbar_arrive_expect_tx(fb, kTileBytes);
+      for (int c = 0; c < D / 64; ++c) tma_load_4d(sdO + c * kT * 128, &tmdO, fb, c * 64, h, i * kT, b);
       int t = 0;
       for (; t < n; ++t) {
         const int st = t % kStages, use = t / kStages;
         if (use > 0 && !wait_bounded(smem_addr(&sy.empty[st]), (use - 1) & 1, sy, p)) break;
-        const uint32_t dst = base + st * kStage, bar = smem_addr(&sy.full[st]);
+        const uint32_t dst = sRing + st * kStage, bar = smem_addr(&sy.full[st]);
         mbar_arrive_expect_tx(bar, 2 * kTileBytes);
         for (int c = 0; c < D / 64; ++c) {
           tma_load_4d(dst + c * kT * 128, &tmK, bar, c * 64, kvh, t * kT, b);
           tma_load_4d(dst + kTileBytes + c * kT * 128, &tmV, bar, c * 64, kvh, t * kT, b);
         }
       }
+      wait_drain(fb, 0);
       drain_ring<kStages>(sy, t);
     }
   } else if (warp == kMmaWarp) {
     const bool leader = elect_one();
-    bool ok = __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.a_ready), 0, sy, p));
+    bool ok = __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.a_ready), 0, sy, p)) &&
+              __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.fixed_full), 0, sy, p));
     tc_fence_after_sync();
-    auto stage_of = [&](int t) { return base + (t % kStages) * kStage; };
+    auto stage_of = [&](int t) { return sRing + (t % kStages) * kStage; };
     auto wait_stage = [&](int t) -> bool {
       if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.full[t % kStages]),
                                                 (t / kStages) & 1, sy, p)))
@@ -663,29 +702,36 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
       tc_fence_after_sync();
       return true;
     };
+    auto wait_all = [&](uint64_t& bar, int t) -> bool {
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&bar), t & 1, sy, p))) return false;
+      tc_fence_after_sync();
+      return true;
+    };
     if (ok && (ok = wait_stage(0))) {
-      mma_scores_full<D>(leader, tmem + cS, tmem + cQ, stage_of(0));               // S  = Q K^T
+      mma_scores_full<D>(leader, tmem + cS, tmem + cQ, stage_of(0));           // S  = Q K^T
       if (leader) mma_commit(smem_addr(&sy.s_full[0]));
-      mma_scores_full<D>(leader, tmem + cP, tmem + cO, stage_of(0) + kTileBytes);  // dP = dO V^T
+      mma_scores_full_ss<D>(leader, tmem + cP, sdO, stage_of(0) + kTileBytes);  // dP = dO V^T
       if (leader) mma_commit(smem_addr(&sy.dp_full));
     }
     for (int t = 0; t < n && ok; ++t) {
       const bool more = t + 1 < n;
-      // S(t) consumed: the next tile's scores may overwrite it
-      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.p_full[0]), t & 1, sy, p))) break;
+      // S(t) read out: the next tile's scores may overwrite it
+      if (!wait_all(sy.p_full[0], t)) break;
       if (more) {
         if (!wait_stage(t + 1)) break;
         mma_scores_full<D>(leader, tmem + cS, tmem + cQ, stage_of(t + 1));
         if (leader) mma_commit(smem_addr(&sy.s_full[0]));
       }
-      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.ds_full), t & 1, sy, p))) break;
-      tc_fence_after_sync();
-      mma_accum_full<D>(leader, tmem + cDQ, tmem + cP, stage_of(t), t > 0);        // dQ += dS K
-      if (leader) mma_commit(smem_addr(&sy.empty[t % kStages]));
+      // dP(t) read out: the next tile's dP may overwrite it
+      if (!wait_all(sy.dp_free, t)) break;
       if (more) {
-        mma_scores_full<D>(leader, tmem + cP, tmem + cO, stage_of(t + 1) + kTileBytes);
+        mma_scores_full_ss<D>(leader, tmem + cP, sdO, stage_of(t + 1) + kTileBytes);
         if (leader) mma_commit(smem_addr(&sy.dp_full));
       }
+      if (!wait_all(sy.ds_full, t)) break;
+      mma_accum_dq<D>(leader, tmem + cDQ, tmem + cDS, stage_of(t), t > 0);      // dQ += dS K
+      if (leader) mma_commit(smem_addr(&sy.dq_done));
+      if (leader) mma_commit(smem_addr(&sy.empty[t % kStages]));
     }
     if (leader) mma_commit(smem_addr(&sy.done));
     teardown(sy, p, leader);
@@ -698,8 +744,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
     const int row = i * kT + r;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const size_t qoff = ((static_cast<size_t>(b) * p.L + row) * p.n_q + h) * D;
-    // Q_i (first warpgroup) and dO_i (second) become the A operands in TMEM
-    if (cw < 2) row_to_tmem<D>(lane_base + (cw ? cO : cQ), (cw ? do_rows : q_rows) + qoff, row < p.L);
+    // Q_i becomes the A operand of S in TMEM (first warpgroup)
+    if (cw == 0) row_to_tmem<D>(lane_base + cQ, q_rows + qoff, row < p.L);
     tmem_wait_st();
     tc_fence_before_sync();
     mbar_arrive(smem_addr(&sy.a_ready));
@@ -741,28 +787,38 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
       }
       tc_fence_before_sync();
       mbar_arrive(smem_addr(&sy.p_full[0]));
-      // phase 2: dS = P * (dP - D), written over this warpgroup's consumed dP columns
+      // phase 2: dP read out (its columns are then free for the next tile),
+      // dS = P * (dP - D) into the dS columns once dQ(t-1) has read them
       if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.dp_full), t & 1, sy, p))) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
+      uint32_t dk[kColsQ / 2];
 #pragma unroll
       for (int c = 0; c < kColsQ / 32; ++c) {
         uint32_t dpv[32];
         tmem_ld32(lane_base + cP + k0 + 32 * c, dpv);
         tmem_wait_ld(dpv);
-        uint32_t dk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const uint64_t dd = fadd2(
               f32x2_pack(__uint_as_float(dpv[2 * e]), __uint_as_float(dpv[2 * e + 1])), nd2);
           float d0, d1;
           f32x2_unpack(fmul2(f32x2_pack(pr[32 * c + 2 * e], pr[32 * c + 2 * e + 1]), dd), d0, d1);
-          dk[e] = pack_bf16x2(d0, d1);
+          dk[16 * c + e] = pack_bf16x2(d0, d1);
         }
-        tmem_st16(lane_base + cP + k0 + 16 * c, dk);
       }
+      tc_fence_before_sync();
+      mbar_arrive(smem_addr(&sy.dp_free));
+      if (t > 0 && !__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.dq_done), (t - 1) & 1, sy, p))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+#pragma unroll
+      for (int c = 0; c < kColsQ / 32; ++c)
+        tmem_st16(lane_base + cDS + k0 / 2 + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(dk + 16 * c));
       tmem_wait_st();
       tc_fence_before_sync();
       mbar_arrive(smem_addr(&sy.ds_full));
@@ -791,7 +847,7 @@ EncodeTiledFn g_bwd_encode = nullptr;
 template <int D>
 constexpr int dkdv_smem() { return tile_bytes<D>() + kStagesKV * (2 * tile_bytes<D>() + 1024) + 1024; }
 template <int D>
-constexpr int dq_smem() { return kStages * (2 * tile_bytes<D>()) + 1024; }
+constexpr int dq_smem() { return tile_bytes<D>() + kStages * (2 * tile_bytes<D>()) + 1024; }
 
 attn_status_t bwd_device_ready(cudaStream_t stream, int** status) {
   int dev = 0;
@@ -917,14 +973,14 @@ attn_status_t attn_prefill_bwd(const void* q, const void* k, const void* v, cons
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     dkdv_kernel<128><<<kv_tiles, kThreads, dkdv_smem<128>(), stream>>>(mq, mdo, mv, kh, p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-    dq_kernel<128><<<q_tiles, kThreads, dq_smem<128>(), stream>>>(mk, mv, qh, doh, p);
+    dq_kernel<128><<<q_tiles, kThreads, dq_smem<128>(), stream>>>(mk, mv, mdo, qh, p);
   } else {
     rowdot_kernel<64><<<row_blocks, 256, 0, stream>>>(oh, doh, lse, nlse2, nrowdot,
                                                       static_cast<int>(B), p.L, n_q, Lp);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     dkdv_kernel<64><<<kv_tiles, kThreads, dkdv_smem<64>(), stream>>>(mq, mdo, mv, kh, p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-    dq_kernel<64><<<q_tiles, kThreads, dq_smem<64>(), stream>>>(mk, mv, qh, doh, p);
+    dq_kernel<64><<<q_tiles, kThreads, dq_smem<64>(), stream>>>(mk, mv, mdo, qh, p);
   }
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
