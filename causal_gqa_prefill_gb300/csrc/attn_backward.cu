@@ -15,24 +15,26 @@
 //   dkdv    one CTA per (b, K/V head, 128-key tile j): loops over the g query
 //           heads of the group and the query tiles that see tile j; with the
 //           key dimension on the TMEM lanes it computes S^T = K Q^T and
-//           dP^T = V dO^T (tcgen05, both operands from shared memory), turns
-//           them into P^T and dS^T (bf16, written back into TMEM) and
-//           accumulates dV += P^T dO and dK += dS^T Q (A from TMEM); dK and dV
-//           for the whole group stay in TMEM until the end;
-//   dq      one CTA per (b, query head, 128-row tile i): S = Q K^T and
-//           dP = dO V^T, dS in TMEM, dQ += dS K over the key tiles it sees.
-// Both tile kernels walk their loop in half-steps of 64 score columns (64
-// queries of a query tile in dkdv, 64 keys of a key tile in dq) with two score
-// buffers in TMEM, so the tensor cores compute half-step u+1's scores while
-// the compute warps turn half-step u's into P/dS.
+//           dP^T = V dO^T (tcgen05, both operands from shared memory, K_j and
+//           V_j resident), turns them into P^T and dS^T (bf16, written back
+//           into TMEM) and accumulates dV += P^T dO and dK += dS^T Q (A from
+//           TMEM); dK and dV for the whole group stay in TMEM until the end;
+//   dq      one CTA per (b, query head, 128-row tile i): S = Q K^T (Q_i in
+//           TMEM) and dP = dO V^T (dO_i in shared memory), dS in its own TMEM
+//           columns, dQ += dS K over the key tiles it sees.
+// Both tile kernels step over whole 128-column score tiles (128 queries of a
+// query tile in dkdv, 128 keys of a key tile in dq), so every product is
+// N = 128 (or D) wide, and order their products so that the tensor cores run
+// the next tile's scores while the compute warps turn this tile's into P/dS.
 //
 // Each kernel has a TMA producer warp, an MMA warp (warp-wide loop, one elected
-// issuing lane) and kComputeWGs compute warpgroups that split the 64 columns
-// of a half-step (thread = TMEM lane = tile row; warpgroup w owns columns
-// [w*C, w*C + C), C = 64 / kComputeWGs). A warpgroup writes its bf16 P/dS
-// back over the first C/2 of its own, already consumed, fp32 columns, so no
-// warpgroup ever overwrites columns another one still has to read; the
-// products that consume P/dS take their A operand K-step by K-step from there.
+// issuing lane) and kComputeWGs compute warpgroups that split the 128 columns
+// of a tile (thread = TMEM lane = tile row; warpgroup w owns columns
+// [w*C, w*C + C), C = 128 / kComputeWGs). A warpgroup writes its bf16 P (and
+// in dkdv dS) back over the first C/2 of its own, already consumed, fp32
+// columns, so no warpgroup ever overwrites columns another one still has to
+// read; the products that consume P/dS take their A operand K-step by K-step
+// from there.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -56,9 +58,7 @@ constexpr int kT = 128;                  // rows per query tile and keys per key
 // chunks of 128 rows x 128 bytes, 128-byte swizzled.
 template <int D>
 __host__ __device__ constexpr int tile_bytes() { return kT * D * 2; }
-constexpr int kHalf = 64;                // score columns per half-step
 constexpr int kComputeWGs = 2;           // compute warpgroups
-constexpr int kCols = kHalf / kComputeWGs;   // dK/dV: half-step columns per warpgroup
 constexpr int kColsQ = kT / kComputeWGs;     // dQ: key-tile columns per warpgroup
 constexpr int kComputeThreads = 128 * kComputeWGs;
 constexpr int kLoadWarp = 4 * kComputeWGs, kMmaWarp = kLoadWarp + 1;
@@ -145,29 +145,9 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
 // TMEM column (relative to the score tile's base) holding the bf16 A operand
 // for K step kk (tile columns 16*kk .. 16*kk + 15): warpgroup w packs its
 // columns [w*C, w*C + C) two per 32-bit column starting at column w*C.
-// (C = kCols in the dK/dV kernel, kColsQ in the dQ kernel.)
-template <int C = kCols>
+template <int C>
 __host__ __device__ constexpr uint32_t a_col(int kk) {
   return static_cast<uint32_t>((16 * kk / C) * C + (16 * kk % C) / 2);
-}
-
-// Scores of a half-step: D[128 x 64] = A B^T over K = 128 (d), A a fixed
-// [128 x 128] bf16 operand in TMEM (64 columns, two elements per column), B
-// rows b_row0 .. b_row0 + 63 of a [128 rows x 128] K-major tile in shared memory.
-// The descriptor is built once; later K steps add their byte offset / 16 to
-// its start-address field (shared addresses stay below 2^18, so no carry).
-template <int D>
-__device__ __forceinline__ void mma_scores(bool leader, uint32_t d_tmem, uint32_t a_tmem,
-                                           uint32_t b_smem, int b_row0) {
-  constexpr uint32_t idesc = idesc_bf16_f32(kT, kHalf, false);
-  // the whole warp runs the loop; the elected lane issues (a converged warp
-  // issues tcgen05.mma faster than a lone lane in a divergent branch)
-  const uint64_t b0 = sdesc_sw128(b_smem + b_row0 * 128, 16, 1024);
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * (kT * 128) + (kk & 3) * 32;
-    if (leader) mma_ts(d_tmem, a_tmem + 8 * kk, b0 + (off >> 4), idesc, kk > 0 ? 1u : 0u);
-  }
 }
 
 // This thread's row of a bf16 [B, L, H, D] tensor into D/2 TMEM columns of
@@ -189,21 +169,6 @@ __device__ __forceinline__ void row_to_tmem(uint32_t taddr, const uint16_t* src,
     }
     tmem_st32(taddr + 32 * half, w);
   }
-}
-
-// D[128 x 128] (+)= A B over K = 64: A the bf16 P/dS of a half-step in TMEM
-// (a_col layout), B rows b_row0 .. b_row0 + 63 of a [128 rows x 128] tile,
-// used MN-major (its rows are the K dimension).
-template <int D>
-__device__ __forceinline__ void mma_accum(bool leader, uint32_t d_tmem, uint32_t a_tmem,
-                                          uint32_t b_smem, int b_row0, bool accumulate) {
-  constexpr uint32_t idesc = idesc_bf16_f32(kT, D, true);
-  const uint64_t b0 = sdesc_sw128(b_smem + b_row0 * 128, kT * 128, 1024);
-#pragma unroll
-  for (int kk = 0; kk < kHalf / 16; ++kk)
-    if (leader)
-      mma_ts(d_tmem, a_tmem + a_col(kk), b0 + ((kk * 16 * 128) >> 4), idesc,
-             (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // Scores of a whole tile: D[128 x 128] = A B^T over K = 128, A a fixed operand
@@ -408,32 +373,17 @@ __device__ __forceinline__ void drain_ring(Sync& sy, int issued) {
   }
 }
 
-// SS product for dP^T of a half-step: D[128 x 64] = V_j dO^T over K = 128 (d),
-// both operands K-major tiles in shared memory (B rows b_row0 .. b_row0 + 63).
-template <int D>
-__device__ __forceinline__ void mma_scores_ss(bool leader, uint32_t d_tmem, uint32_t a_smem,
-                                              uint32_t b_smem, int b_row0) {
-  constexpr uint32_t idesc = idesc_bf16_f32(kT, kHalf, false);
-  const uint64_t a0 = sdesc_sw128(a_smem, 16, 1024);
-  const uint64_t b0 = sdesc_sw128(b_smem + b_row0 * 128, 16, 1024);
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = ((kk >> 2) * (kT * 128) + (kk & 3) * 32) >> 4;
-    if (leader) mma_ss(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
-  }
-}
-
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
-            const __grid_constant__ CUtensorMap tmV, const uint16_t* __restrict__ k_rows,
+            const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
             const BwdParams p) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Sync sy;
-  // smem: V_j | kStagesKV x [Q_i | dO_i | -LSE*log2 e [128] | -D [128]]
+  // smem: K_j | V_j | kStagesKV x [Q_i | dO_i | -LSE*log2 e [128] | -D [128]]
   constexpr int kTileBytes = tile_bytes<D>();
   const uint32_t base = (smem_addr(dyn_smem) + 1023u) & ~1023u;
-  const uint32_t sV = base, sRing = base + kTileBytes;
+  const uint32_t sK = base, sV = base + kTileBytes, sRing = base + 2 * kTileBytes;
   constexpr uint32_t kStage = 2 * kTileBytes + 1024;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int groups = static_cast<int>(gridDim.x) / p.T;
@@ -442,20 +392,22 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   const int b = grp / p.n_kv, kvh = grp - b * p.n_kv;
   const int i0 = p.causal ? j : 0;
   const int nsteps = p.g * (p.T - i0);                 // (head, query tile) pairs
-  const int nhalf = 2 * nsteps;                        // half-steps of 64 queries
   setup(sy);
   const uint32_t tmem = sy.tmem_base;
-  // TMEM columns: K_j 0..D/2-1 (A operand), S^T of half-step u in buffer
-  // u&1 at 64 + 64*(u&1) (P^T is written over it), dP^T 192..255 (dS^T over
-  // it), dV at 256 and dK at 256 + D (D columns each). With two S^T buffers
-  // the tensor cores compute S^T(u+1) while the compute warps are still on u.
-  constexpr uint32_t cK = 0, cS = 64, cP = 192, cDV = 256, cDK = 256 + D;
+  // TMEM columns: S^T 0..127 (P^T, bf16, is written over it), dP^T 128..255
+  // (dS^T over it), dV at 256 and dK at 256 + D (D columns each). Each step
+  // is a whole 128-query tile, so every product has N = 128 (or D): the
+  // tensor cores get 64-cycle MMAs, which one issuing thread keeps up with.
+  constexpr uint32_t cS = 0, cP = 128, cDV = 256, cDK = 256 + D;
 
   if (warp == kLoadWarp) {
     if (lane == 0) {
       const uint32_t fb = smem_addr(&sy.fixed_full);
-      mbar_arrive_expect_tx(fb, kTileBytes);
-      for (int c = 0; c < D / 64; ++c) tma_load_4d(sV + c * kT * 128, &tmV, fb, c * 64, kvh, j * kT, b);
+      mbar_arrive_expect_tx(fb, 2 * kTileBytes);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_4d(sK + c * kT * 128, &tmK, fb, c * 64, kvh, j * kT, b);
+        tma_load_4d(sV + c * kT * 128, &tmV, fb, c * 64, kvh, j * kT, b);
+      }
       int t = 0;
       for (; t < nsteps; ++t) {
         const int st = t % kStagesKV, use = t / kStagesKV;
@@ -477,77 +429,64 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     }
   } else if (warp == kMmaWarp) {
     const bool leader = elect_one();
-    bool ok = __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.a_ready), 0, sy, p)) &&
-              __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.fixed_full), 0, sy, p));
+    bool ok = __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.fixed_full), 0, sy, p));
     tc_fence_after_sync();
-    auto stage_of = [&](int u) { return sRing + ((u >> 1) % kStagesKV) * kStage; };
-    auto wait_stage = [&](int u) -> bool {
-      if (u & 1) return true;   // the second half uses the stage the first one waited for
-      const int t = u >> 1;
+    auto stage_of = [&](int t) { return sRing + (t % kStagesKV) * kStage; };
+    auto wait_stage = [&](int t) -> bool {
       if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.full[t % kStagesKV]),
                                                 (t / kStagesKV) & 1, sy, p)))
         return false;
       tc_fence_after_sync();
       return true;
     };
-    auto issue_st = [&](int u) {      // S^T(u) = K Q^T into buffer u&1
-      mma_scores<D>(leader, tmem + cS + 64 * (u & 1), tmem + cK, stage_of(u), 64 * (u & 1));
-      if (leader) mma_commit(smem_addr(&sy.s_full[u & 1]));
-    };
-    auto issue_dpt = [&](int u) {     // dP^T(u) = V dO^T
-      mma_scores_ss<D>(leader, tmem + cP, sV, stage_of(u) + kTileBytes, 64 * (u & 1));
-      if (leader) mma_commit(smem_addr(&sy.dp_full));
+    auto wait_all = [&](uint64_t& bar, int t) -> bool {
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&bar), t & 1, sy, p))) return false;
+      tc_fence_after_sync();
+      return true;
     };
     if (ok && (ok = wait_stage(0))) {
-      issue_st(0);
-      issue_dpt(0);
+      mma_scores_full_ss<D>(leader, tmem + cS, sK, stage_of(0));                  // S^T  = K Q^T
+      if (leader) mma_commit(smem_addr(&sy.s_full[0]));
+      mma_scores_full_ss<D>(leader, tmem + cP, sV, stage_of(0) + kTileBytes);     // dP^T = V dO^T
+      if (leader) mma_commit(smem_addr(&sy.dp_full));
     }
-    for (int u = 0; u < nhalf && ok; ++u) {
-      const uint32_t sQ = stage_of(u), sdO = sQ + kTileBytes;
-      const int r0 = 64 * (u & 1);
-      const bool more = u + 1 < nhalf;
-      // S^T(u+1) goes into the buffer that held half-step u-1, whose P^T the
-      // previously issued dV(u-1) reads first (the tensor cores run in order)
+    for (int t = 0; t < nsteps && ok; ++t) {
+      const uint32_t sQ = stage_of(t), sdO = sQ + kTileBytes;
+      const bool more = t + 1 < nsteps;
+      if (!wait_all(sy.p_full[0], t)) break;
+      mma_accum_full<D>(leader, tmem + cDV, tmem + cS, sdO, t > 0);              // dV += P^T dO
+      // S^T(t+1) overwrites P^T(t), which the dV product issued above reads first
       if (more) {
-        if (!wait_stage(u + 1)) break;
-        issue_st(u + 1);
+        if (!wait_stage(t + 1)) break;
+        mma_scores_full_ss<D>(leader, tmem + cS, sK, stage_of(t + 1));
+        if (leader) mma_commit(smem_addr(&sy.s_full[0]));
       }
-      // one P-ready barrier per S^T buffer: the compute warps may finish P^T(u+1)
-      // before this wait runs, which a single barrier could not tell apart
-      if (!__all_sync(0xffffffffu,
-                      wait_bounded(smem_addr(&sy.p_full[u & 1]), (u >> 1) & 1, sy, p)))
-        break;
-      tc_fence_after_sync();
-      mma_accum<D>(leader, tmem + cDV, tmem + cS + 64 * (u & 1), sdO, r0, u > 0);   // dV += P^T dO
-      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.ds_full), u & 1, sy, p))) break;
-      tc_fence_after_sync();
-      mma_accum<D>(leader, tmem + cDK, tmem + cP, sQ, r0, u > 0);                   // dK += dS^T Q
-      if (leader && (u & 1)) mma_commit(smem_addr(&sy.empty[(u >> 1) % kStagesKV]));
-      if (more) issue_dpt(u + 1);
+      if (!wait_all(sy.ds_full, t)) break;
+      mma_accum_full<D>(leader, tmem + cDK, tmem + cP, sQ, t > 0);               // dK += dS^T Q
+      if (leader) mma_commit(smem_addr(&sy.empty[t % kStagesKV]));
+      if (more) {
+        mma_scores_full_ss<D>(leader, tmem + cP, sV, stage_of(t + 1) + kTileBytes);
+        if (leader) mma_commit(smem_addr(&sy.dp_full));
+      }
     }
     if (leader) mma_commit(smem_addr(&sy.done));
     teardown(sy, p, leader);
     return;
   } else if (warp < 4 * kComputeWGs) {
     // compute warpgroups: thread r = key row r of the tile = TMEM lane r;
-    // warpgroup cw takes query columns [cw*kCols, cw*kCols + kCols) of a half-step
+    // warpgroup cw takes query columns [cw*kColsQ, cw*kColsQ + kColsQ) of a step
     const int cw = warp >> 2;
     const int r = (warp & 3) * 32 + lane;
     const int krow = j * kT + r;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    // K_j becomes the A operand of S^T in TMEM (first warpgroup)
     const size_t koff = ((static_cast<size_t>(b) * p.L + krow) * p.n_kv + kvh) * D;
-    if (cw == 0) row_to_tmem<D>(lane_base + cK, k_rows + koff, krow < p.L);
-    tmem_wait_st();
-    tc_fence_before_sync();
-    mbar_arrive(smem_addr(&sy.a_ready));
     const uint64_t c2 = f32x2_pack(p.c, p.c);
+    const int q0 = cw * kColsQ;                        // first query column (in the tile)
     bool ok = true;
-    for (int u = 0; u < nhalf; ++u) {
-      const int t = u >> 1, st = t % kStagesKV;
+    for (int t = 0; t < nsteps; ++t) {
+      const int st = t % kStagesKV;
       const int i = i0 + t % (p.T - i0);
-      if (!__all_sync(0xffffffffu,
-                      wait_bounded(smem_addr(&sy.s_full[u & 1]), (u >> 1) & 1, sy, p)) ||
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.s_full[0]), t & 1, sy, p)) ||
           // the staged row statistics arrived with the stage's copies
           !__all_sync(0xffffffffu,
                       wait_bounded(smem_addr(&sy.full[st]), (t / kStagesKV) & 1, sy, p))) {
@@ -555,22 +494,22 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         break;
       }
       tc_fence_after_sync();
-      const int q0 = 64 * (u & 1) + cw * kCols;        // first query column (in the tile)
       const float4* nl4 = reinterpret_cast<const float4*>(
           dyn_smem + (sRing + st * kStage + 2 * kTileBytes - smem_addr(dyn_smem))) + q0 / 4;
       const float4* nd4 = nl4 + 32;
       const bool diag = p.causal && i == j;           // query c < key r is masked
-      const uint32_t sbuf = lane_base + cS + 64 * (u & 1) + cw * kCols;
-      // phase 1: P^T from S^T, kept in registers for phase 2
-      float pr[kCols];
-      {
+      // phase 1: P^T from S^T, kept in registers for phase 2, and written (bf16)
+      // over this warpgroup's first consumed S^T columns
+      float pr[kColsQ];
+#pragma unroll
+      for (int cc = 0; cc < kColsQ / 32; ++cc) {
         uint32_t sv[32];
-        tmem_ld32(sbuf, sv);
+        tmem_ld32(lane_base + cS + q0 + 32 * cc, sv);
         tmem_wait_ld(sv);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float4 nl = nl4[e];
+          const float4 nl = nl4[8 * cc + e];
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
             const int jj = 4 * e + 2 * h2;
@@ -580,33 +519,34 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             f32x2_unpack(x, x0, x1);
             float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
             if (diag) {
-              if (q0 + jj < r) p0 = 0.0f;
-              if (q0 + jj + 1 < r) p1 = 0.0f;
+              if (q0 + 32 * cc + jj < r) p0 = 0.0f;
+              if (q0 + 32 * cc + jj + 1 < r) p1 = 0.0f;
             }
-            pr[jj] = p0;
-            pr[jj + 1] = p1;
+            pr[32 * cc + jj] = p0;
+            pr[32 * cc + jj + 1] = p1;
             pk[jj / 2] = pack_bf16x2(p0, p1);
           }
         }
-        tmem_st16(sbuf, pk);                           // over this warpgroup's consumed S^T columns
-        tmem_wait_st();
-        tc_fence_before_sync();
-        mbar_arrive(smem_addr(&sy.p_full[u & 1]));
+        tmem_st16(lane_base + cS + q0 + 16 * cc, pk);
       }
-      // phase 2: dS^T = P^T * (dP^T - D)
-      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.dp_full), u & 1, sy, p))) {
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(smem_addr(&sy.p_full[0]));
+      // phase 2: dS^T = P^T * (dP^T - D), over this warpgroup's consumed dP^T columns
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.dp_full), t & 1, sy, p))) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      {
+#pragma unroll
+      for (int cc = 0; cc < kColsQ / 32; ++cc) {
         uint32_t dpv[32];
-        tmem_ld32(lane_base + cP + cw * kCols, dpv);
+        tmem_ld32(lane_base + cP + q0 + 32 * cc, dpv);
         tmem_wait_ld(dpv);
         uint32_t dk[16];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float4 nd = nd4[e];
+          const float4 nd = nd4[8 * cc + e];
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
             const int jj = 4 * e + 2 * h2;
@@ -614,15 +554,15 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                 f32x2_pack(__uint_as_float(dpv[jj]), __uint_as_float(dpv[jj + 1])),
                 h2 ? f32x2_pack(nd.z, nd.w) : f32x2_pack(nd.x, nd.y));
             float d0, d1;
-            f32x2_unpack(fmul2(f32x2_pack(pr[jj], pr[jj + 1]), dd), d0, d1);
+            f32x2_unpack(fmul2(f32x2_pack(pr[32 * cc + jj], pr[32 * cc + jj + 1]), dd), d0, d1);
             dk[jj / 2] = pack_bf16x2(d0, d1);
           }
         }
-        tmem_st16(lane_base + cP + cw * kCols, dk);   // over this warpgroup's consumed dP^T columns
-        tmem_wait_st();
-        tc_fence_before_sync();
-        mbar_arrive(smem_addr(&sy.ds_full));
+        tmem_st16(lane_base + cP + q0 + 16 * cc, dk);
       }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(smem_addr(&sy.ds_full));
     }
     if (ok && __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.done), 0, sy, p))) {
       tc_fence_after_sync();
@@ -845,7 +785,7 @@ std::mutex g_bwd_mutex;
 bool g_bwd_ready[kMaxDevices];
 EncodeTiledFn g_bwd_encode = nullptr;
 template <int D>
-constexpr int dkdv_smem() { return tile_bytes<D>() + kStagesKV * (2 * tile_bytes<D>() + 1024) + 1024; }
+constexpr int dkdv_smem() { return 2 * tile_bytes<D>() + kStagesKV * (2 * tile_bytes<D>() + 1024) + 1024; }
 template <int D>
 constexpr int dq_smem() { return tile_bytes<D>() + kStages * (2 * tile_bytes<D>()) + 1024; }
 
@@ -962,7 +902,6 @@ attn_status_t attn_prefill_bwd(const void* q, const void* k, const void* v, cons
       static_cast<unsigned>((rows + kRowdotRowsPerBlock - 1) / kRowdotRowsPerBlock);
   const uint16_t* oh = static_cast<const uint16_t*>(o);
   const uint16_t* qh = static_cast<const uint16_t*>(q);
-  const uint16_t* kh = static_cast<const uint16_t*>(k);
   const uint16_t* doh = static_cast<const uint16_t*>(dout);
   const int Lp = static_cast<int>(T * kT);
   const unsigned kv_tiles = static_cast<unsigned>(B * n_kv * T);
@@ -971,14 +910,14 @@ attn_status_t attn_prefill_bwd(const void* q, const void* k, const void* v, cons
     rowdot_kernel<128><<<row_blocks, 256, 0, stream>>>(oh, doh, lse, nlse2, nrowdot,
                                                        static_cast<int>(B), p.L, n_q, Lp);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-    dkdv_kernel<128><<<kv_tiles, kThreads, dkdv_smem<128>(), stream>>>(mq, mdo, mv, kh, p);
+    dkdv_kernel<128><<<kv_tiles, kThreads, dkdv_smem<128>(), stream>>>(mq, mdo, mk, mv, p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     dq_kernel<128><<<q_tiles, kThreads, dq_smem<128>(), stream>>>(mk, mv, mdo, qh, p);
   } else {
     rowdot_kernel<64><<<row_blocks, 256, 0, stream>>>(oh, doh, lse, nlse2, nrowdot,
                                                       static_cast<int>(B), p.L, n_q, Lp);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-    dkdv_kernel<64><<<kv_tiles, kThreads, dkdv_smem<64>(), stream>>>(mq, mdo, mv, kh, p);
+    dkdv_kernel<64><<<kv_tiles, kThreads, dkdv_smem<64>(), stream>>>(mq, mdo, mk, mv, p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     dq_kernel<64><<<q_tiles, kThreads, dq_smem<64>(), stream>>>(mk, mv, mdo, qh, p);
   }
