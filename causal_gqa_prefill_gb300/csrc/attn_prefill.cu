@@ -30,6 +30,9 @@
 //   [128,256) S1 / P1
 //   [256,384) O0 accumulator (D columns)
 //   [384,512) O1 accumulator
+// Shared memory (d_h = 128, bf16): Q0 and Q1 (32 KiB each), a 4-stage K/V
+// ring (32 KiB per tile) and 4 KiB per softmax warp through which the
+// epilogue turns each thread's O row into row-contiguous global stores.
 //
 // MMA issue order per key tile j (ping-pong between the two query tiles, so
 // one tile's softmax overlaps the other tile's matrix products):
@@ -61,6 +64,8 @@ constexpr int kOtherRegs = 56;      // per thread, warpgroup 2
 constexpr int kRegBudget = 2 * 128 * kSoftmaxRegs + 128 * kOtherRegs;
 static_assert(kRegBudget <= kThreads * 168, "setmaxnreg split exceeds the launch allocation");
 constexpr int kLoadWarp = 8;
+constexpr int kOStageWarpBytes = 32 * 128;           // 32 rows x 128 bytes per softmax warp
+constexpr int kOStageBytes = 8 * kOStageWarpBytes;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384;
@@ -81,7 +86,9 @@ struct Tile {
   static constexpr int kQBytes = kBM * kRowBytes;
   static constexpr int kKVBytes = kBN * kRowBytes;
   static constexpr int kStages = (kKVBytes == 32768) ? 4 : 8;   // K/V ring depth (K and V share it)
-  static constexpr int kSmemBytes = 2 * kQBytes + kStages * kKVBytes + 1024;
+  // two Q tiles, the K/V ring, and 4 KiB per softmax warp to stage O rows
+  // for coalesced stores
+  static constexpr int kSmemBytes = 2 * kQBytes + kStages * kKVBytes + kOStageBytes + 1024;
   // MMA K step: 16 bf16 or 32 e4m3 elements, 32 bytes either way.
   static constexpr int kKStep = 32 / kElemBytes;
   static_assert(kRowBytes % 128 == 0, "rows must fill whole 128-byte swizzle chunks");
@@ -382,6 +389,19 @@ __device__ void mma_role(Ctl& ctl, const Params& p, uint32_t tmem, uint32_t sQ0,
 
 // ------------------------------------------------------------------- softmax
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -401,7 +421,8 @@ __device__ __forceinline__ float row_max128(const float* v) {
 }
 
 template <int D, bool F8>
-__device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem) {
+__device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem,
+                             uint32_t o_stage) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = (warp & 3) * 32 + lane;                         // tile row = TMEM lane
   const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
@@ -530,22 +551,41 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem)
     tc_fence_after_sync();
     const float inv_l = p.o_scale / l_run;
     const bool valid = row < p.Lq;
-    uint16_t* orow = p.o + ((static_cast<size_t>(x.b) * p.Lq + row) * p.n_q + x.head[slot]) *
-                               static_cast<size_t>(D);
+    // O rows leave through this warp's 4 KiB of shared memory, 64 columns (128
+    // bytes of bf16) at a time: each thread writes its own row's 128 bytes
+    // (16-byte unit u at u ^ (row % 8), so a warp's stores hit all banks), then
+    // each store to global memory covers four whole rows' 128-byte pieces
+    // (eight threads per row) instead of 32 scattered 16-byte pieces.
+    const uint32_t stg = o_stage + warp * kOStageWarpBytes;
+    const int row0 = x.qtile[slot] * kBM + (warp & 3) * 32;    // first row of this warp
+    const size_t hstride = static_cast<size_t>(p.n_q) * D;     // elements between rows
+    uint16_t* obase = p.o + (static_cast<size_t>(x.b) * p.Lq * p.n_q + x.head[slot]) *
+                                static_cast<size_t>(D);
+#pragma unroll 1
+    for (int hh = 0; hh < D / 64; ++hh) {
 #pragma unroll
-    for (int c = 0; c < D; c += 32) {
-      uint32_t ov[32];
-      tmem_ld32(tO + c, ov);
-      tmem_wait_ld(ov);
-      uint32_t w[16];
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t ov[32];
+        tmem_ld32(tO + 64 * hh + 32 * c2, ov);
+        tmem_wait_ld(ov);
+        uint32_t w[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        w[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
-      if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + c);
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        for (int u = 4 * c2; u < 4 * c2 + 4; ++u)
+          st_shared_v4(stg + lane * 128 + ((u ^ (lane & 7)) << 4), w[4 * u - 16 * c2],
+                       w[4 * u - 16 * c2 + 1], w[4 * u - 16 * c2 + 2], w[4 * u - 16 * c2 + 3]);
       }
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int rr = 4 * k + (lane >> 3), u = lane & 7;
+        const uint4 v = ld_shared_v4(stg + rr * 128 + ((u ^ (rr & 7)) << 4));
+        if (row0 + rr < p.Lq)
+          *reinterpret_cast<uint4*>(obase + static_cast<size_t>(row0 + rr) * hstride + 64 * hh + 8 * u) = v;
+      }
+      __syncwarp();
     }
     if (valid) {
       const float m_fin = (m_run == -INFINITY) ? 0.0f : m_run;
@@ -601,7 +641,7 @@ attn_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
 
   if (warp < 8) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
-    softmax_role<D, F8>(warp >> 2, ctl, p, tmem);
+    softmax_role<D, F8>(warp >> 2, ctl, p, tmem, sKV + TL::kStages * TL::kKVBytes);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
     if (warp == kLoadWarp) {
