@@ -392,6 +392,9 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   const int b = grp / p.n_kv, kvh = grp - b * p.n_kv;
   const int i0 = p.causal ? j : 0;
   const int nsteps = p.g * (p.T - i0);                 // (head, query tile) pairs
+  // The dQ kernel (this grid's programmatic dependent) reads nothing this
+  // kernel writes: its CTAs may take SMs as soon as every CTA here has started.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   setup(sy);
   const uint32_t tmem = sy.tmem_base;
   // TMEM columns: S^T 0..127 (P^T, bf16, is written over it), dP^T 128..255
@@ -821,6 +824,26 @@ attn_status_t bwd_device_ready(cudaStream_t stream, int** status) {
   return ATTN_OK;
 }
 
+// dQ is launched as the dK/dV kernel's programmatic dependent: it reads only
+// the inputs and the row statistics (complete before dK/dV started), so it
+// needs no grid-dependency wait and fills the SMs that dK/dV's last CTAs free.
+template <int D>
+cudaError_t launch_dq(unsigned grid, cudaStream_t stream, const CUtensorMap& mk,
+                      const CUtensorMap& mv, const CUtensorMap& mdo, const uint16_t* qh,
+                      const BwdParams& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = dq_smem<D>();
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, dq_kernel<D>, mk, mv, mdo, qh, p);
+}
+
 bool encode_tile_map(CUtensorMap* map, const void* ptr, int D, int H, int64_t L, int64_t B) {
   const cuuint64_t d = static_cast<cuuint64_t>(D);
   const cuuint64_t dims[4] = {d, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(L),
@@ -912,14 +935,14 @@ attn_status_t attn_prefill_bwd(const void* q, const void* k, const void* v, cons
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     dkdv_kernel<128><<<kv_tiles, kThreads, dkdv_smem<128>(), stream>>>(mq, mdo, mk, mv, p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-    dq_kernel<128><<<q_tiles, kThreads, dq_smem<128>(), stream>>>(mk, mv, mdo, qh, p);
+    if (launch_dq<128>(q_tiles, stream, mk, mv, mdo, qh, p) != cudaSuccess) return ATTN_ERR_CUDA;
   } else {
     rowdot_kernel<64><<<row_blocks, 256, 0, stream>>>(oh, doh, lse, nlse2, nrowdot,
                                                       static_cast<int>(B), p.L, n_q, Lp);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     dkdv_kernel<64><<<kv_tiles, kThreads, dkdv_smem<64>(), stream>>>(mq, mdo, mk, mv, p);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-    dq_kernel<64><<<q_tiles, kThreads, dq_smem<64>(), stream>>>(mk, mv, mdo, qh, p);
+    if (launch_dq<64>(q_tiles, stream, mk, mv, mdo, qh, p) != cudaSuccess) return ATTN_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
