@@ -288,6 +288,72 @@ __device__ __forceinline__ void store_chunk(uint32_t taddr, uint16_t* dst, float
   }
 }
 
+// dK/dV phase 1 for one warpgroup: P^T = 2^(c S^T + nl) for its kColsQ query
+// columns of this thread's key row (S^T read from TMEM at `taddr`, the row
+// statistics nl from shared memory), kept in `pr` and written back as bf16
+// over the first consumed columns. kMask: the diagonal tile, where query
+// column q0 + k is masked when q0 + k < r (q_minus_r = q0 - r).
+template <bool kMask>
+__device__ __forceinline__ void pt_from_st(uint32_t taddr, const float4* nl4, uint64_t c2,
+                                           int q_minus_r, float (&pr)[kColsQ]) {
+#pragma unroll
+  for (int cc = 0; cc < kColsQ / 32; ++cc) {
+    uint32_t sv[32];
+    tmem_ld32(taddr + 32 * cc, sv);
+    tmem_wait_ld(sv);
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float4 nl = nl4[8 * cc + e];
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int jj = 4 * e + 2 * h2;
+        const uint64_t x = ffma2(f32x2_pack(__uint_as_float(sv[jj]), __uint_as_float(sv[jj + 1])),
+                                 c2, h2 ? f32x2_pack(nl.z, nl.w) : f32x2_pack(nl.x, nl.y));
+        float x0, x1;
+        f32x2_unpack(x, x0, x1);
+        float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        if (kMask) {
+          if (q_minus_r + 32 * cc + jj < 0) p0 = 0.0f;
+          if (q_minus_r + 32 * cc + jj + 1 < 0) p1 = 0.0f;
+        }
+        pr[32 * cc + jj] = p0;
+        pr[32 * cc + jj + 1] = p1;
+        pk[jj / 2] = pack_bf16x2(p0, p1);
+      }
+    }
+    tmem_st16(taddr + 16 * cc, pk);
+  }
+}
+
+// dQ phase 1 for one warpgroup: P = 2^(c S + nl) for its kColsQ key columns
+// [k0, k0 + kColsQ) of this thread's query row, kept in `pr`. kMask: keys
+// after in-tile index `keep` are masked (the diagonal tile, or keys past L).
+template <bool kMask>
+__device__ __forceinline__ void p_from_s(uint32_t taddr, uint64_t c2, uint64_t nl2, int k0,
+                                         int keep, float (&pr)[kColsQ]) {
+#pragma unroll
+  for (int c = 0; c < kColsQ / 32; ++c) {
+    uint32_t sv[32];
+    tmem_ld32(taddr + 32 * c, sv);
+    tmem_wait_ld(sv);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const uint64_t x = ffma2(
+          f32x2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), c2, nl2);
+      float x0, x1;
+      f32x2_unpack(x, x0, x1);
+      float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+      if (kMask) {
+        if (k0 + 32 * c + 2 * e > keep) p0 = 0.0f;
+        if (k0 + 32 * c + 2 * e + 1 > keep) p1 = 0.0f;
+      }
+      pr[32 * c + 2 * e] = p0;
+      pr[32 * c + 2 * e + 1] = p1;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ rowdot
 
 // Half a warp per padded row (b, h, t), t < Lp: 16 lanes x 8 dimensions, with
@@ -504,34 +570,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       // phase 1: P^T from S^T, kept in registers for phase 2, and written (bf16)
       // over this warpgroup's first consumed S^T columns
       float pr[kColsQ];
-#pragma unroll
-      for (int cc = 0; cc < kColsQ / 32; ++cc) {
-        uint32_t sv[32];
-        tmem_ld32(lane_base + cS + q0 + 32 * cc, sv);
-        tmem_wait_ld(sv);
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float4 nl = nl4[8 * cc + e];
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int jj = 4 * e + 2 * h2;
-            const uint64_t x = ffma2(f32x2_pack(__uint_as_float(sv[jj]), __uint_as_float(sv[jj + 1])),
-                                     c2, h2 ? f32x2_pack(nl.z, nl.w) : f32x2_pack(nl.x, nl.y));
-            float x0, x1;
-            f32x2_unpack(x, x0, x1);
-            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            if (diag) {
-              if (q0 + 32 * cc + jj < r) p0 = 0.0f;
-              if (q0 + 32 * cc + jj + 1 < r) p1 = 0.0f;
-            }
-            pr[32 * cc + jj] = p0;
-            pr[32 * cc + jj + 1] = p1;
-            pk[jj / 2] = pack_bf16x2(p0, p1);
-          }
-        }
-        tmem_st16(lane_base + cS + q0 + 16 * cc, pk);
-      }
+      // the causal mask only touches the diagonal tile: a separate copy of the
+      // loop keeps its compares and selects out of every other tile
+      if (diag) pt_from_st<true>(lane_base + cS + q0, nl4, c2, q0 - r, pr);
+      else pt_from_st<false>(lane_base + cS + q0, nl4, c2, q0 - r, pr);
       tmem_wait_st();
       tc_fence_before_sync();
       mbar_arrive(smem_addr(&sy.p_full[0]));
@@ -708,26 +750,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
       const bool masked = p.causal ? (t == i) : (p.L - t * kT < kT);
       const int keep = p.causal ? r : p.L - 1 - t * kT;
       float pr[kColsQ];
-#pragma unroll
-      for (int c = 0; c < kColsQ / 32; ++c) {
-        uint32_t sv[32];
-        tmem_ld32(lane_base + cS + k0 + 32 * c, sv);
-        tmem_wait_ld(sv);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const uint64_t x = ffma2(
-              f32x2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), c2, nl2);
-          float x0, x1;
-          f32x2_unpack(x, x0, x1);
-          float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          if (masked) {
-            if (k0 + 32 * c + 2 * e > keep) p0 = 0.0f;
-            if (k0 + 32 * c + 2 * e + 1 > keep) p1 = 0.0f;
-          }
-          pr[32 * c + 2 * e] = p0;
-          pr[32 * c + 2 * e + 1] = p1;
-        }
-      }
+      if (masked) p_from_s<true>(lane_base + cS + k0, c2, nl2, k0, keep, pr);
+      else p_from_s<false>(lane_base + cS + k0, c2, nl2, k0, keep, pr);
       tc_fence_before_sync();
       mbar_arrive(smem_addr(&sy.p_full[0]));
       // phase 2: dP read out (its columns are then free for the next tile),
