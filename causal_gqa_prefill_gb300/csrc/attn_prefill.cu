@@ -420,7 +420,7 @@ __device__ __forceinline__ float row_max128(const float* v) {
   return max3(max3(m[0], m[1], m[2]), max3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
 }
 
-template <int D, bool F8>
+template <int D, bool F8, bool kPos>
 __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem,
                              uint32_t o_stage) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -431,7 +431,7 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem,
   const uint32_t bar_s = smem_addr(&ctl.s_full[slot]);
   const uint32_t bar_p = smem_addr(&ctl.p_full[slot]);
   const uint32_t bar_o = smem_addr(&ctl.o_done[slot]);
-  const float cc = p.scale_pos ? p.c : 1.0f;
+  const float cc = kPos ? p.c : 1.0f;
   const uint64_t cc2 = f32x2_pack(cc, cc);
   uint32_t ph_s = 0, ph_o = 0;
 
@@ -459,9 +459,10 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem,
         tmem_after_wait(*reinterpret_cast<uint32_t(*)[32]>(sr + 64));
         tmem_after_wait(*reinterpret_cast<uint32_t(*)[32]>(sr + 96));
       }
-      if (!p.scale_pos) {
-        // Non-positive scale: fold it in first so that masking and the
-        // maximum below work on the scaled scores (then cc = 1).
+      if (!kPos) {
+        // Non-positive scale (its own kernel instance): fold it in first so
+        // that masking and the maximum below work on the scaled scores (then
+        // cc = 1).
 #pragma unroll
         for (int i = 0; i < 128; ++i) s[i] *= p.c;
       }
@@ -482,17 +483,6 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem,
       if (need) {
         alpha = ex2_approx(m_run - m_new);
         m_run = m_new;
-      }
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-#pragma unroll
-        for (int c = 0; c < D; c += 32) {
-          uint32_t ov[32];
-          tmem_ld32(tO + c, ov);
-          tmem_wait_ld(ov);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-          tmem_st32(tO + c, ov);
-        }
       }
       // P = 2^(c*s - m) into the first columns of this tile's S region (every
       // score of the row is already in registers): bf16 pairs in [0, 64), or
@@ -541,6 +531,21 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem,
       float sa, sb;
       f32x2_unpack(sum2, sa, sb);
       l_run = l_run * alpha + (sa + sb);
+      // O <- O * 2^(m_old - m_new) when some row's maximum moved (rare): done
+      // after P, when the row's scores are no longer held in registers, and
+      // before the P-ready arrival that lets O += P V run (O already holds
+      // every earlier tile: S of this tile was issued after the last P V).
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t ov[32];
+          tmem_ld32(tO + c, ov);
+          tmem_wait_ld(ov);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tmem_st32(tO + c, ov);
+        }
+      }
       tmem_wait_st();
       tc_fence_before_sync();
       mbar_arrive(bar_p);
@@ -597,7 +602,7 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem,
 
 // -------------------------------------------------------------------- kernel
 
-template <int D, bool F8>
+template <int D, bool F8, bool kPos>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
@@ -641,7 +646,7 @@ attn_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
 
   if (warp < 8) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
-    softmax_role<D, F8>(warp >> 2, ctl, p, tmem, sKV + TL::kStages * TL::kKVBytes);
+    softmax_role<D, F8, kPos>(warp >> 2, ctl, p, tmem, sKV + TL::kStages * TL::kKVBytes);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
     if (warp == kLoadWarp) {
@@ -680,21 +685,22 @@ EncodeTiledFn g_encode = nullptr;
 // The softmax warpgroups raise their register limit with setmaxnreg; that
 // only succeeds if the CTA was launched with at least kRegBudget registers,
 // so refuse to launch a build whose register count does not cover the split.
-template <int D, bool F8>
+template <int D, bool F8, bool kPos>
 bool configure_kernel() {
   cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, attn_prefill_fwd_kernel<D, F8>) != cudaSuccess ||
+  if (cudaFuncGetAttributes(&fa, attn_prefill_fwd_kernel<D, F8, kPos>) != cudaSuccess ||
       fa.numRegs * kThreads < kRegBudget)
     return false;
-  return cudaFuncSetAttribute(attn_prefill_fwd_kernel<D, F8>,
+  return cudaFuncSetAttribute(attn_prefill_fwd_kernel<D, F8, kPos>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               Tile<D, F8>::kSmemBytes) == cudaSuccess;
 }
 
 // Register-split check and shared-memory limit for every kernel instance.
 bool configure_kernels() {
-  return configure_kernel<64, false>() && configure_kernel<128, false>() &&
-         configure_kernel<128, true>();
+  return configure_kernel<64, false, true>() && configure_kernel<128, false, true>() &&
+         configure_kernel<128, true, true>() && configure_kernel<64, false, false>() &&
+         configure_kernel<128, false, false>() && configure_kernel<128, true, false>();
 }
 
 attn_status_t device_state(cudaStream_t stream, DeviceState** out) {
@@ -789,6 +795,23 @@ attn_status_t validate(const void* q, const void* k, const void* v, const void* 
   return ATTN_OK;
 }
 
+// One launch of the kernel instance for (f8, d_h) and the sign of the scale:
+// a positive scale multiplies inside the exponent's FMA, any other is applied
+// to the scores first (separate instances, so neither pays for the other).
+template <bool kPos>
+void launch_instance(int grid, cudaStream_t stream, const CUtensorMap& mq, const CUtensorMap& mk,
+                     const CUtensorMap& mv, const Params& p, bool f8, int d_h) {
+  if (f8)
+    attn_prefill_fwd_kernel<128, true, kPos>
+        <<<grid, kThreads, Tile<128, true>::kSmemBytes, stream>>>(mq, mk, mv, p);
+  else if (d_h == 128)
+    attn_prefill_fwd_kernel<128, false, kPos>
+        <<<grid, kThreads, Tile<128, false>::kSmemBytes, stream>>>(mq, mk, mv, p);
+  else
+    attn_prefill_fwd_kernel<64, false, kPos>
+        <<<grid, kThreads, Tile<64, false>::kSmemBytes, stream>>>(mq, mk, mv, p);
+}
+
 // Encodes the tensor maps, fills the parameters and launches (arguments
 // already validated). `status` is the device status word the kernel reports
 // wait timeouts into; `sms` the device's multiprocessor count.
@@ -827,15 +850,10 @@ attn_status_t launch_forward(const void* q, const void* k, const void* v, void* 
   p.spin_limit = kSpinLimitCycles;
 
   const int grid = units < sms ? units : sms;
-  if (f8)
-    attn_prefill_fwd_kernel<128, true>
-        <<<grid, kThreads, Tile<128, true>::kSmemBytes, stream>>>(mq, mk, mv, p);
-  else if (d_h == 128)
-    attn_prefill_fwd_kernel<128, false>
-        <<<grid, kThreads, Tile<128, false>::kSmemBytes, stream>>>(mq, mk, mv, p);
+  if (p.scale_pos)
+    launch_instance<true>(grid, stream, mq, mk, mv, p, f8, d_h);
   else
-    attn_prefill_fwd_kernel<64, false>
-        <<<grid, kThreads, Tile<64, false>::kSmemBytes, stream>>>(mq, mk, mv, p);
+    launch_instance<false>(grid, stream, mq, mk, mv, p, f8, d_h);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
