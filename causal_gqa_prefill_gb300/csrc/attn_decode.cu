@@ -276,6 +276,10 @@ attn_decode_split_kernel(const __grid_constant__ CUtensorMap tmQ,
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = ctl.tmem_base;
+  // Launched as the programmatic dependent of the stream's previous kernel
+  // (the previous call's combine, or whatever wrote Q, K and V): the set-up
+  // above overlaps it; global memory is touched only after it has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == kLoadWarp) {
     if (lane == 0) {
@@ -544,14 +548,10 @@ attn_decode_split_kernel(const __grid_constant__ CUtensorMap tmQ,
 
 // One CTA of kCombineWarps warps per (b, query head): O = sum_s w_s O_s,
 // w_s = exp(lse_s - LSE) over the head's segments (the CTAs whose tile ranges
-// cover its K/V head). The warps take interleaved segments, each lane four
-// dimensions; their sums are added in shared memory.
+// cover its K/V head). One pass: the warps take interleaved segments and merge
+// them against a running maximum, each lane four dimensions; the warps' states
+// are merged in shared memory.
 constexpr int kCombineWarps = 8;
-__device__ __forceinline__ size_t segment_row(const DecodeParams& p, long long hd, int r,
-                                              long long c) {
-  const long long slot = hd - range_start(c, p.W, p.G) / p.T;
-  return static_cast<size_t>((c * p.P_max + slot) * p.g + r);
-}
 
 __global__ void __launch_bounds__(32 * kCombineWarps)
 attn_decode_combine_kernel(uint16_t* o, float* lse, const DecodeParams p) {
@@ -563,47 +563,55 @@ attn_decode_combine_kernel(uint16_t* o, float* lse, const DecodeParams p) {
   const long long hd = static_cast<long long>(b) * p.n_kv + h / p.g;
   const long long c0 = cta_of(hd * p.T, p.W, p.G);
   const int ns = static_cast<int>(cta_of(hd * p.T + p.T - 1, p.W, p.G) - c0 + 1);
+  // The head is segment slot `slot0` of CTA c0; every later CTA's range starts
+  // inside the head (each range holds at least one tile), so it is their slot 0.
+  const long long slot0 = hd - range_start(c0, p.W, p.G) / p.T;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // The next kernel in the stream (the next call's split kernel) may launch
+  // and set up now; it waits for this grid to complete before touching
+  // global memory.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // Launched early behind the split kernel: wait until it has completed and
   // its partial results are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  float mx = -INFINITY;
-  for (int s = threadIdx.x; s < ns; s += blockDim.x)
-    mx = fmaxf(mx, p.part_lse[segment_row(p, hd, r, c0 + s)]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  if (lane == 0) red_m[warp] = mx;
-  __syncthreads();
-  mx = red_m[0];
-#pragma unroll
-  for (int w = 1; w < kCombineWarps; ++w) mx = fmaxf(mx, red_m[w]);
+  float m = -INFINITY, wsum = 0.0f;
   float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  float wsum = 0.0f;
 #pragma unroll 4
   for (int s = warp; s < ns; s += kCombineWarps) {
-    const size_t sr = segment_row(p, hd, r, c0 + s);
-    const float w = __expf(p.part_lse[sr] - mx);
+    const size_t sr = static_cast<size_t>(((c0 + s) * p.P_max + (s == 0 ? slot0 : 0)) * p.g + r);
+    const float ls = p.part_lse[sr];
     const float4 v = *reinterpret_cast<const float4*>(p.part_o + sr * kDim + 4 * lane);
-    wsum += w;
-    acc.x = fmaf(w, v.x, acc.x);
-    acc.y = fmaf(w, v.y, acc.y);
-    acc.z = fmaf(w, v.z, acc.z);
-    acc.w = fmaf(w, v.w, acc.w);
+    const float mn = fmaxf(m, ls);
+    const float a = (m == -INFINITY) ? 0.0f : __expf(m - mn);
+    const float w = __expf(ls - mn);
+    m = mn;
+    wsum = fmaf(wsum, a, w);
+    acc.x = fmaf(w, v.x, acc.x * a);
+    acc.y = fmaf(w, v.y, acc.y * a);
+    acc.z = fmaf(w, v.z, acc.z * a);
+    acc.w = fmaf(w, v.w, acc.w * a);
   }
   red_o[warp][lane] = acc;
-  if (lane == 0) red_w[warp] = wsum;
+  if (lane == 0) {
+    red_m[warp] = m;
+    red_w[warp] = wsum;
+  }
   __syncthreads();
   if (warp == 0) {
-    float4 t = red_o[0][lane];
-    float ws = red_w[0];
+    float mx = red_m[0];
 #pragma unroll
-    for (int w = 1; w < kCombineWarps; ++w) {
+    for (int w = 1; w < kCombineWarps; ++w) mx = fmaxf(mx, red_m[w]);
+    float4 t = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    float ws = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) {
+      const float a = (red_m[w] == -INFINITY) ? 0.0f : __expf(red_m[w] - mx);
       const float4 u = red_o[w][lane];
-      t.x += u.x;
-      t.y += u.y;
-      t.z += u.z;
-      t.w += u.w;
-      ws += red_w[w];
+      t.x = fmaf(a, u.x, t.x);
+      t.y = fmaf(a, u.y, t.y);
+      t.z = fmaf(a, u.z, t.z);
+      t.w = fmaf(a, u.w, t.w);
+      ws = fmaf(a, red_w[w], ws);
     }
     const float inv = 1.0f / ws;
     const uint32_t w0 = pack_bf16x2(t.x * inv, t.y * inv);
@@ -753,26 +761,31 @@ attn_status_t attn_decode_fwd(const void* q, const void* k, const void* v, void*
   p.P_max = static_cast<int>(s.P_max);
   p.c = scale * 1.4426950408889634f;
   p.spin_limit = 1ll << 31;   // about a second at 2 GHz
-  const unsigned grid = static_cast<unsigned>(s.G);
-  if (p.g <= 4)
-    attn_decode_split_kernel<4><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
-  else if (p.g <= 8)
-    attn_decode_split_kernel<8><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
-  else
-    attn_decode_split_kernel<16><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
-  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-  // The combine is the split kernel's programmatic dependent: its CTAs are
-  // scheduled while the split kernel still runs and start at its completion.
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(B * n_q));
-  cfg.blockDim = dim3(32 * kCombineWarps);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
+  // Both kernels are launched as programmatic dependents of the kernel before
+  // them in the stream: the split kernel's set-up overlaps the previous
+  // kernel's end, and the combine's CTAs are scheduled while the split kernel
+  // still runs. Each waits (griddepcontrol.wait) before touching memory.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(s.G));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  cudaError_t e;
+  if (p.g <= 4)
+    e = cudaLaunchKernelEx(&cfg, attn_decode_split_kernel<4>, mq, mk, mv, p);
+  else if (p.g <= 8)
+    e = cudaLaunchKernelEx(&cfg, attn_decode_split_kernel<8>, mq, mk, mv, p);
+  else
+    e = cudaLaunchKernelEx(&cfg, attn_decode_split_kernel<16>, mq, mk, mv, p);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  cfg.gridDim = dim3(static_cast<unsigned>(B * n_q));
+  cfg.blockDim = dim3(32 * kCombineWarps);
+  cfg.dynamicSmemBytes = 0;
   uint16_t* o16 = static_cast<uint16_t*>(o);
   if (cudaLaunchKernelEx(&cfg, attn_decode_combine_kernel, o16, lse, p) != cudaSuccess)
     return ATTN_ERR_CUDA;

@@ -75,6 +75,31 @@ def test_decode_workspace_is_reused():
         check_full(q, k, v, o, lse, what=f"reuse {seed}")
 
 
+def test_decode_back_to_back_calls():
+    """Calls queued on one stream with one workspace and no host sync between
+    them. Each call's kernels are programmatic dependents of the kernel before
+    them: the next call's split kernel sets up while this call's combine still
+    reads the partial results, and the cache is rewritten by a kernel right
+    before each call. Every call must still see its own inputs and partials."""
+    B, Lk, n_q, n_kv = 2, 20000, 6, 3          # ranges cross head boundaries
+    w = W.custom(B, 1, n_q, n_kv, 128, Lk=Lk)
+    ws = torch.empty(attn_decode_workspace_bytes(B, Lk, n_q, n_kv), dtype=torch.uint8,
+                     device="cuda")
+    inputs = [W.make_inputs(w, "cuda", seed=s) for s in (21, 22, 23, 24)]
+    kbuf = torch.empty_like(inputs[0][1])
+    vbuf = torch.empty_like(inputs[0][2])
+    torch.cuda.synchronize()
+    outs = []
+    for q, k, v in inputs:
+        torch.mul(k, 1.0, out=kbuf)             # an elementwise kernel writes the cache
+        torch.mul(v, 1.0, out=vbuf)
+        outs.append(attn_decode(q, kbuf, vbuf, workspace=ws))
+    torch.cuda.synchronize()
+    assert attn_device_check() == ATTN_OK
+    for i, ((q, k, v), (o, lse)) in enumerate(zip(inputs, outs)):
+        check_full(q, k, v, o, lse, what=f"call {i}")
+
+
 @pytest.mark.parametrize("num", [10, 11])
 def test_decode_workloads(num):
     w = W.WORKLOADS[num]
