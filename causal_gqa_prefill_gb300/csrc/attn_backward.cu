@@ -825,6 +825,12 @@ attn_status_t bwd_device_ready(cudaStream_t stream, int** status) {
   if (ds != ATTN_OK) return ds;
   std::lock_guard<std::mutex> lock(g_bwd_mutex);
   if (!g_bwd_ready[dev]) {
+    // one-time set-up: not inside a stream capture
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+      cudaGetLastError();
+      return ATTN_ERR_UNSUPPORTED;
+    }
     if (!g_bwd_encode) {
       cudaDriverEntryPointQueryResult q;
       void* fn = nullptr;

@@ -647,6 +647,12 @@ attn_status_t decode_device_ready(cudaStream_t stream, int** status) {
   if (ds != ATTN_OK) return ds;
   std::lock_guard<std::mutex> lock(g_decode_mutex);
   if (g_decode_ready[dev]) return ATTN_OK;
+  // one-time set-up: not inside a stream capture
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+    cudaGetLastError();
+    return ATTN_ERR_UNSUPPORTED;
+  }
   if (!g_decode_encode) {
     cudaDriverEntryPointQueryResult q;
     void* fn = nullptr;

@@ -710,6 +710,14 @@ attn_status_t device_state(cudaStream_t stream, DeviceState** out) {
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceState& st = g_dev[dev];
   if (!st.ready) {
+    // The set-up allocates and clears the status word on `stream`; neither
+    // may happen inside a stream capture, so a first call there is refused
+    // (and leaves nothing half set up).
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+      cudaGetLastError();
+      return ATTN_ERR_UNSUPPORTED;
+    }
     int major = 0, minor = 0, sms = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||

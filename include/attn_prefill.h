@@ -37,6 +37,16 @@
  * stream). The call returns after the launch is enqueued; o and lse are valid
  * once the stream has reached that point. q, k, v are not modified. Results
  * are deterministic: the same inputs give bit-identical o and lse.
+ *
+ * CUDA graphs: the first call of each family (forward, decode, backward) on a
+ * device does a one-time set-up and must not be made while a stream capture
+ * is under way; made there, it returns ATTN_ERR_UNSUPPORTED and sets up
+ * nothing. After it, every compute entry point can be captured with the
+ * stream it is given (attn_decode_fwd as two kernel nodes joined by a
+ * programmatic dependency); replaying the graph recomputes from whatever the
+ * captured input buffers hold then. attn_device_check synchronizes and cannot
+ * be captured; attn_prefill_fwd_host uses its own streams and is not meant
+ * for capture.
  */
 #ifndef ATTN_PREFILL_H
 #define ATTN_PREFILL_H
@@ -53,7 +63,8 @@ typedef enum {
                                 Lk < Lq, non-finite scale, causal not 0/1,
                                 misaligned pointer */
   ATTN_ERR_UNSUPPORTED = 2,  /* d_h not 64 or 128 (128 for fp8), sizes beyond 32-bit
-                                tile indexing, device that is not sm_103 */
+                                tile indexing, device that is not sm_103, a first
+                                call on a device made during stream capture */
   ATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call or the launch failed */
   ATTN_ERR_TIMEOUT = 4       /* a kernel wait ran past its limit (reported by
                                 attn_device_check); outputs of that launch are
