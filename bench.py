@@ -254,6 +254,26 @@ def oracle_backward_sample(w, q_host, k_host, v_host, do_host, rng, rows, second
     return flops, spent, done
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (x86) or implementer and part codes (Arm)."""
+    import platform
+
+    try:
+        with open("/proc/cpuinfo") as f:
+            fields = [ln.split(":", 1) for ln in f.read().splitlines() if ":" in ln]
+    except OSError:
+        return platform.machine()
+    kv = {}
+    for k, v in fields:
+        kv.setdefault(k.strip(), v.strip())
+    if "model name" in kv:
+        return kv["model name"]
+    if "CPU part" in kv:
+        return "%s, CPU implementer %s, part %s" % (
+            platform.machine(), kv.get("CPU implementer", "?"), kv["CPU part"])
+    return platform.machine()
+
+
 def blas_threads() -> int:
     try:
         from threadpoolctl import threadpool_info
@@ -312,6 +332,7 @@ def run_reference(args, w, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": dict(w.describe()),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "cpu_model": cpu_model(),
                          "sample": f"{rows_per_step} random query rows per step of {w.name}; "
                                    "fp64 NumPy oracle on the host cores"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -354,6 +375,7 @@ def run_reference_backward(args, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": dict(w.describe()),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "cpu_model": cpu_model(),
                          "sample": f"backward of the first {rows} positions of one random "
                                    f"(batch, K/V head) group per step of {w.name}; fp64 NumPy "
                                    "oracle on the host cores"},
@@ -625,7 +647,8 @@ def run_ours(args, w, dist):
         "roofline": roof or {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                              "frac": achieved / peak, "peak_source": peak_note,
                              "traffic": traffic},
-        "step_ms_min": None if window else min(step_ms), "wall_s_timed": t_wall,
+        "step_ms_min": None if window else min(step_ms),
+        "step_ms_median": None if window else statistics.median(step_ms), "wall_s_timed": t_wall,
         "grid": cg.attn_prefill_grid_size(w.B, w.L, w.n_q, w.n_kv, w.d_h, w.causal),
     }
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline and w.backward:
@@ -635,6 +658,7 @@ def run_ours(args, w, dist):
         f, s, n = oracle_backward_sample(w, fq, fk, fv, fd, rng, rows, seconds=args.cpu_seconds)
         line["cpu_baseline"] = {
             "value": f / s / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": f"backward of the first {rows} positions of {n} random (batch, K/V head) "
                       f"groups of {w.name} (fp64 NumPy oracle), {s:.1f} s"}
     elif dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
@@ -643,6 +667,7 @@ def run_ours(args, w, dist):
         f, s, n = oracle_sample(w, fq, fk, fv, rng, 256, seconds=args.cpu_seconds)
         line["cpu_baseline"] = {
             "value": f / s / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": f"{n} random query rows of {w.name} (fp64 NumPy oracle), {s:.1f} s"}
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
