@@ -357,8 +357,12 @@ __device__ __forceinline__ void p_from_s(uint32_t taddr, uint64_t c2, uint64_t n
 // ------------------------------------------------------------------ rowdot
 
 // Half a warp per padded row (b, h, t), t < Lp: 16 lanes x 8 dimensions, with
-// 16-byte loads; a warp takes four rows so that its loads of all four are in
-// flight together. Rows past L get -inf and 0 without touching O or dO.
+// 16-byte loads; a warp takes four rows at a time so that its loads of all
+// four are in flight together, and walks the rows grid-stride (at most eight
+// blocks per SM: a long-lived grid instead of thousands of short blocks).
+// Rows past L get -inf and 0 without touching O or dO. The dK/dV kernel is
+// launched as this grid's programmatic dependent and waits for it before it
+// reads the statistics.
 constexpr int kRowdotRowsPerWarp = 4;
 __device__ __forceinline__ float dot2_bf16(uint32_t a, uint32_t d, float acc) {
   acc = fmaf(__uint_as_float(a << 16), __uint_as_float(d << 16), acc);
@@ -381,9 +385,13 @@ __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 d) {
 template <int D>
 __global__ void rowdot_kernel(const uint16_t* o, const uint16_t* dout, const float* lse,
                               float* nlse2, float* nrowdot, int B, int L, int n_q, int Lp) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t total = static_cast<int64_t>(B) * n_q * Lp;
-  const int64_t warp_id = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t warps = (total + kRowdotRowsPerWarp - 1) / kRowdotRowsPerWarp;
+  const int64_t wstride = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int half = (threadIdx.x >> 4) & 1, l16 = threadIdx.x & 15;
+  for (int64_t warp_id = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       warp_id < warps; warp_id += wstride) {
   uint4 a[kRowdotRowsPerWarp / 2], d[kRowdotRowsPerWarp / 2];
   bool live[kRowdotRowsPerWarp / 2];
 #pragma unroll
@@ -425,6 +433,7 @@ __global__ void rowdot_kernel(const uint16_t* o, const uint16_t* dout, const flo
       nlse2[row] = (t < L) ? -lse[(row / Lp) * L + t] * kLog2e : -INFINITY;
     }
   }
+  }
 }
 
 // -------------------------------------------------------------------- dK, dV
@@ -458,10 +467,14 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   const int b = grp / p.n_kv, kvh = grp - b * p.n_kv;
   const int i0 = p.causal ? j : 0;
   const int nsteps = p.g * (p.T - i0);                 // (head, query tile) pairs
-  // The dQ kernel (this grid's programmatic dependent) reads nothing this
-  // kernel writes: its CTAs may take SMs as soon as every CTA here has started.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   setup(sy);
+  // Launched as the row kernel's programmatic dependent: the set-up above
+  // overlaps its end; the row statistics are read only after it completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The dQ kernel (this grid's programmatic dependent) reads nothing this
+  // kernel writes: its CTAs may take SMs as soon as every CTA here is past
+  // the wait above (so the row statistics are complete when dQ starts).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const uint32_t tmem = sy.tmem_base;
   // TMEM columns: S^T 0..127 (P^T, bf16, is written over it), dP^T 128..255
   // (dS^T over it), dV at 256 and dK at 256 + D (D columns each). Each step
@@ -858,6 +871,23 @@ attn_status_t bwd_device_ready(cudaStream_t stream, int** status) {
 // the inputs and the row statistics (complete before dK/dV started), so it
 // needs no grid-dependency wait and fills the SMs that dK/dV's last CTAs free.
 template <int D>
+cudaError_t launch_dkdv(unsigned grid, cudaStream_t stream, const CUtensorMap& mq,
+                        const CUtensorMap& mdo, const CUtensorMap& mk, const CUtensorMap& mv,
+                        const BwdParams& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = dkdv_smem<D>();
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, dkdv_kernel<D>, mq, mdo, mk, mv, p);
+}
+
+template <int D>
 cudaError_t launch_dq(unsigned grid, cudaStream_t stream, const CUtensorMap& mk,
                       const CUtensorMap& mv, const CUtensorMap& mdo, const uint16_t* qh,
                       const BwdParams& p) {
@@ -951,8 +981,12 @@ attn_status_t attn_prefill_bwd(const void* q, const void* k, const void* v, cons
 
   const int64_t rows = B * n_q * T * kT;
   constexpr int kRowdotRowsPerBlock = 8 * kRowdotRowsPerWarp;   // 256 threads
-  const unsigned row_blocks =
-      static_cast<unsigned>((rows + kRowdotRowsPerBlock - 1) / kRowdotRowsPerBlock);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    sms = 1;
+  const int64_t need_blocks = (rows + kRowdotRowsPerBlock - 1) / kRowdotRowsPerBlock;
+  const unsigned row_blocks = static_cast<unsigned>(need_blocks < 8 * sms ? need_blocks : 8 * sms);
   const uint16_t* oh = static_cast<const uint16_t*>(o);
   const uint16_t* qh = static_cast<const uint16_t*>(q);
   const uint16_t* doh = static_cast<const uint16_t*>(dout);
@@ -963,15 +997,13 @@ attn_status_t attn_prefill_bwd(const void* q, const void* k, const void* v, cons
     rowdot_kernel<128><<<row_blocks, 256, 0, stream>>>(oh, doh, lse, nlse2, nrowdot,
                                                        static_cast<int>(B), p.L, n_q, Lp);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-    dkdv_kernel<128><<<kv_tiles, kThreads, dkdv_smem<128>(), stream>>>(mq, mdo, mk, mv, p);
-    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    if (launch_dkdv<128>(kv_tiles, stream, mq, mdo, mk, mv, p) != cudaSuccess) return ATTN_ERR_CUDA;
     if (launch_dq<128>(q_tiles, stream, mk, mv, mdo, qh, p) != cudaSuccess) return ATTN_ERR_CUDA;
   } else {
     rowdot_kernel<64><<<row_blocks, 256, 0, stream>>>(oh, doh, lse, nlse2, nrowdot,
                                                       static_cast<int>(B), p.L, n_q, Lp);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-    dkdv_kernel<64><<<kv_tiles, kThreads, dkdv_smem<64>(), stream>>>(mq, mdo, mk, mv, p);
-    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    if (launch_dkdv<64>(kv_tiles, stream, mq, mdo, mk, mv, p) != cudaSuccess) return ATTN_ERR_CUDA;
     if (launch_dq<64>(q_tiles, stream, mk, mv, mdo, qh, p) != cudaSuccess) return ATTN_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
