@@ -149,3 +149,37 @@ def test_first_call_during_capture_is_refused():
     for fam in ("fwd", "dec", "bwd"):
         assert res[fam + "_capture"] == ATTN_ERR_UNSUPPORTED, res
         assert res[fam + "_eager"] == ATTN_OK, res
+
+
+def test_concurrent_streams_match_sequential_calls():
+    """The same calls issued on two streams with no ordering between them
+    (each stream with its own workspaces and outputs) give the bits they give
+    one after another: no state of one call leaks into the other."""
+    a, b = _make(41), _make(42)
+    o_a, l_a = attn_prefill(a[0], a[1], a[2])
+    o_b, l_b = attn_prefill(b[0], b[1], b[2])
+    torch.cuda.synchronize()
+
+    def calls(x, o_f, l_f):
+        q, k, v, qc, qd, do = x
+        o, lse = attn_prefill(q, k, v)
+        od, ld = attn_decode(qd, k, v)
+        grads = attn_prefill_backward(q, k, v, o_f, l_f, do)
+        return (o, lse, od, ld) + tuple(grads)
+
+    seq = [calls(a, o_a, l_a), calls(b, o_b, l_b)]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    par = []
+    for _ in range(3):                     # several rounds so the calls overlap on the GPU
+        par = []
+        for s, (x, o_f, l_f) in zip(streams, ((a, o_a, l_a), (b, o_b, l_b))):
+            with torch.cuda.stream(s):
+                par.append(calls(x, o_f, l_f))
+    torch.cuda.synchronize()
+    assert attn_device_check() == ATTN_OK
+    for got, want in zip(par, seq):
+        for g, w in zip(got, want):
+            assert torch.equal(g, w)
