@@ -19,9 +19,11 @@
 //           V_j resident), turns them into P^T and dS^T (bf16, written back
 //           into TMEM) and accumulates dV += P^T dO and dK += dS^T Q (A from
 //           TMEM); dK and dV for the whole group stay in TMEM until the end;
-//   dq      one CTA per (b, query head, 128-row tile i): S = Q K^T (Q_i in
+//   dq      persistent (one CTA per SM), walking (b, query head, 128-row
+//           tile i) units longest first in snake order: S = Q K^T (Q_i in
 //           TMEM) and dP = dO V^T (dO_i in shared memory), dS in its own TMEM
-//           columns, dQ += dS K over the key tiles it sees.
+//           columns, dQ += dS K over the key tiles it sees; the next unit's
+//           K/V tiles stream in while the current unit drains.
 // Both tile kernels step over whole 128-column score tiles (128 queries of a
 // query tile in dkdv, 128 keys of a key tile in dq), so every product is
 // N = 128 (or D) wide, and order their products so that the tensor cores run
@@ -79,6 +81,7 @@ struct BwdParams {
   uint16_t* dk;             // bf16 [B, L, n_kv, 128]
   uint16_t* dv;
   int* status;
+  int q_units;              // dQ work units: B * n_q * T query tiles
 };
 
 constexpr int kStages = 3;               // dQ: ring of streamed K/V tiles
@@ -640,6 +643,31 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
 
 // ------------------------------------------------------------------------ dQ
 
+// dQ unit u (longest first): query tile i = T - 1 - u / groups of head
+// (b, h) = u % groups, groups = B * n_q.
+struct DqUnit {
+  int b, h, i, n;
+};
+__device__ __forceinline__ DqUnit dq_unit(int u, const BwdParams& p) {
+  const int groups = p.q_units / p.T;
+  DqUnit x;
+  x.i = p.T - 1 - u / groups;
+  const int grp = u - (p.T - 1 - x.i) * groups;
+  x.b = grp / p.n_q;
+  x.h = grp - x.b * p.n_q;
+  x.n = p.causal ? x.i + 1 : p.T;
+  return x;
+}
+
+// Persistent: one CTA per SM walks the units in snake order (round r takes
+// units r*G .. r*G+G-1, left to right on even rounds, right to left on odd
+// ones), so each CTA's set-up happens once and the next unit's K/V tiles
+// stream in while the current one drains.
+__device__ __forceinline__ int dq_snake(int r) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return r * G + ((r & 1) ? (G - 1 - c) : c);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -653,85 +681,119 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
   const uint32_t sdO = base, sRing = base + kTileBytes;
   constexpr uint32_t kStage = 2 * kTileBytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int groups = static_cast<int>(gridDim.x) / p.T;   // B * n_q
-  const int i = p.T - 1 - static_cast<int>(blockIdx.x) / groups;   // longest first
-  const int grp = blockIdx.x - (p.T - 1 - i) * groups;
-  const int b = grp / p.n_q, h = grp - b * p.n_q;
-  const int kvh = h / p.g;
-  const int n = p.causal ? i + 1 : p.T;                // key tiles
+  const int units = p.q_units;
+  const int G = static_cast<int>(gridDim.x);
   setup(sy);
   const uint32_t tmem = sy.tmem_base;
   // TMEM columns: Q_i at 0 (D/2 columns, the A operand of S), S 64..191,
   // dP 192..319, dS 320..383 (bf16, two keys per column), dQ 384..511.
   // dP is read out before dS is formed and dS has its own columns, so per key
   // tile t the tensor cores run S(t+1) and dP(t+1) while the compute warps
-  // still work on tile t, and dQ(t) as soon as dS(t) is in.
+  // still work on tile t, and dQ(t) as soon as dS(t) is in. Barrier phases
+  // count tiles and units over the CTA's whole walk.
   constexpr uint32_t cQ = 0, cS = 64, cP = 192, cDS = 320, cDQ = 384;
 
   if (warp == kLoadWarp) {
     if (lane == 0) {
       const uint32_t fb = smem_addr(&sy.fixed_full);
-      mbar_arrive_expect_tx(fb, kTileBytes);
-      for (int c = 0; c < D / 64; ++c) tma_load_4d(sdO + c * kT * 128, &tmdO, fb, c * 64, h, i * kT, b);
-      int t = 0;
-      for (; t < n; ++t) {
-        const int st = t % kStages, use = t / kStages;
-        if (use > 0 && !wait_bounded(smem_addr(&sy.empty[st]), (use - 1) & 1, sy, p)) break;
-        const uint32_t dst = sRing + st * kStage, bar = smem_addr(&sy.full[st]);
-        mbar_arrive_expect_tx(bar, 2 * kTileBytes);
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_4d(dst + c * kT * 128, &tmK, bar, c * 64, kvh, t * kT, b);
-          tma_load_4d(dst + kTileBytes + c * kT * 128, &tmV, bar, c * 64, kvh, t * kT, b);
+      int it = 0, uc = 0;
+      bool ok = true;
+      for (int r = 0; r * G < units && ok; ++r) {
+        const int u = dq_snake(r);
+        if (u >= units) continue;
+        const DqUnit x = dq_unit(u, p);
+        const int kvh = x.h / p.g;
+        // The first ring's worth of this unit's K/V tiles goes out while the
+        // previous unit still runs; dO_i's buffer is free only once every
+        // product of the previous unit is done.
+        const int pre = x.n < kStages ? x.n : kStages;
+        for (int t = 0; t < x.n; ++t, ++it) {
+          if (t == pre) {
+            if (uc > 0 && !wait_bounded(smem_addr(&sy.done), (uc - 1) & 1, sy, p)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(fb, kTileBytes);
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_4d(sdO + c * kT * 128, &tmdO, fb, c * 64, x.h, x.i * kT, x.b);
+            ++uc;
+          }
+          const int st = it % kStages, use = it / kStages;
+          if (use > 0 && !wait_bounded(smem_addr(&sy.empty[st]), (use - 1) & 1, sy, p)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = sRing + st * kStage, bar = smem_addr(&sy.full[st]);
+          mbar_arrive_expect_tx(bar, 2 * kTileBytes);
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_4d(dst + c * kT * 128, &tmK, bar, c * 64, kvh, t * kT, x.b);
+            tma_load_4d(dst + kTileBytes + c * kT * 128, &tmV, bar, c * 64, kvh, t * kT, x.b);
+          }
+        }
+        if (ok && pre == x.n) {
+          // every tile fitted in the ring ahead of dO
+          if (uc > 0 && !wait_bounded(smem_addr(&sy.done), (uc - 1) & 1, sy, p)) break;
+          mbar_arrive_expect_tx(fb, kTileBytes);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(sdO + c * kT * 128, &tmdO, fb, c * 64, x.h, x.i * kT, x.b);
+          ++uc;
         }
       }
-      wait_drain(fb, 0);
-      drain_ring<kStages>(sy, t);
+      if (uc > 0) wait_drain(fb, (uc - 1) & 1);
+      drain_ring<kStages>(sy, it);
     }
   } else if (warp == kMmaWarp) {
     const bool leader = elect_one();
-    bool ok = __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.a_ready), 0, sy, p)) &&
-              __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.fixed_full), 0, sy, p));
-    tc_fence_after_sync();
-    auto stage_of = [&](int t) { return sRing + (t % kStages) * kStage; };
-    auto wait_stage = [&](int t) -> bool {
-      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.full[t % kStages]),
-                                                (t / kStages) & 1, sy, p)))
-        return false;
+    int it = 0, gt = 0, uc = 0;      // ring items, tiles, units consumed so far
+    bool ok = true;
+    auto wait_all = [&](uint64_t& bar, int ph) -> bool {
+      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&bar), ph & 1, sy, p))) return false;
       tc_fence_after_sync();
       return true;
     };
-    auto wait_all = [&](uint64_t& bar, int t) -> bool {
-      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&bar), t & 1, sy, p))) return false;
-      tc_fence_after_sync();
-      return true;
-    };
-    if (ok && (ok = wait_stage(0))) {
+    for (int r = 0; r * G < units && ok; ++r) {
+      const int u = dq_snake(r);
+      if (u >= units) continue;
+      const int n = dq_unit(u, p).n;
+      auto stage_of = [&](int t) { return sRing + ((it + t) % kStages) * kStage; };
+      auto wait_stage = [&](int t) -> bool {
+        return wait_all(sy.full[(it + t) % kStages], (it + t) / kStages);
+      };
+      // Q_i in TMEM (compute threads) and dO_i in shared memory
+      if (!wait_all(sy.a_ready, uc) || !wait_all(sy.fixed_full, uc) || !wait_stage(0)) {
+        ok = false;
+        break;
+      }
       mma_scores_full<D>(leader, tmem + cS, tmem + cQ, stage_of(0));           // S  = Q K^T
       if (leader) mma_commit(smem_addr(&sy.s_full[0]));
       mma_scores_full_ss<D>(leader, tmem + cP, sdO, stage_of(0) + kTileBytes);  // dP = dO V^T
       if (leader) mma_commit(smem_addr(&sy.dp_full));
-    }
-    for (int t = 0; t < n && ok; ++t) {
-      const bool more = t + 1 < n;
-      // S(t) read out: the next tile's scores may overwrite it
-      if (!wait_all(sy.p_full[0], t)) break;
-      if (more) {
-        if (!wait_stage(t + 1)) break;
-        mma_scores_full<D>(leader, tmem + cS, tmem + cQ, stage_of(t + 1));
-        if (leader) mma_commit(smem_addr(&sy.s_full[0]));
+      for (int t = 0; t < n; ++t) {
+        const bool more = t + 1 < n;
+        // S(t) read out: the next tile's scores may overwrite it
+        if (!wait_all(sy.p_full[0], gt + t)) { ok = false; break; }
+        if (more) {
+          if (!wait_stage(t + 1)) { ok = false; break; }
+          mma_scores_full<D>(leader, tmem + cS, tmem + cQ, stage_of(t + 1));
+          if (leader) mma_commit(smem_addr(&sy.s_full[0]));
+        }
+        // dP(t) read out: the next tile's dP may overwrite it
+        if (!wait_all(sy.dp_free, gt + t)) { ok = false; break; }
+        if (more) {
+          mma_scores_full_ss<D>(leader, tmem + cP, sdO, stage_of(t + 1) + kTileBytes);
+          if (leader) mma_commit(smem_addr(&sy.dp_full));
+        }
+        if (!wait_all(sy.ds_full, gt + t)) { ok = false; break; }
+        mma_accum_dq<D>(leader, tmem + cDQ, tmem + cDS, stage_of(t), t > 0);      // dQ += dS K
+        if (leader) mma_commit(smem_addr(&sy.dq_done));
+        if (leader) mma_commit(smem_addr(&sy.empty[(it + t) % kStages]));
       }
-      // dP(t) read out: the next tile's dP may overwrite it
-      if (!wait_all(sy.dp_free, t)) break;
-      if (more) {
-        mma_scores_full_ss<D>(leader, tmem + cP, sdO, stage_of(t + 1) + kTileBytes);
-        if (leader) mma_commit(smem_addr(&sy.dp_full));
-      }
-      if (!wait_all(sy.ds_full, t)) break;
-      mma_accum_dq<D>(leader, tmem + cDQ, tmem + cDS, stage_of(t), t > 0);      // dQ += dS K
-      if (leader) mma_commit(smem_addr(&sy.dq_done));
-      if (leader) mma_commit(smem_addr(&sy.empty[t % kStages]));
+      if (!ok) break;
+      if (leader) mma_commit(smem_addr(&sy.done));
+      it += n;
+      gt += n;
+      ++uc;
     }
-    if (leader) mma_commit(smem_addr(&sy.done));
     teardown(sy, p, leader);
     return;
   } else if (warp < 4 * kComputeWGs) {
@@ -739,76 +801,86 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
     // warpgroup cw takes key columns [cw*kColsQ, cw*kColsQ + kColsQ)
     const int cw = warp >> 2;
     const int r = (warp & 3) * 32 + lane;
-    const int row = i * kT + r;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const size_t qoff = ((static_cast<size_t>(b) * p.L + row) * p.n_q + h) * D;
-    // Q_i becomes the A operand of S in TMEM (first warpgroup)
-    if (cw == 0) row_to_tmem<D>(lane_base + cQ, q_rows + qoff, row < p.L);
-    tmem_wait_st();
-    tc_fence_before_sync();
-    mbar_arrive(smem_addr(&sy.a_ready));
-    const size_t srow = (static_cast<size_t>(b) * p.n_q + h) * (p.T * kT) + row;
-    const float nl = p.nlse2[srow], nd = p.nrowdot[srow];
-    const uint64_t c2 = f32x2_pack(p.c, p.c), nl2 = f32x2_pack(nl, nl), nd2 = f32x2_pack(nd, nd);
+    const uint64_t c2 = f32x2_pack(p.c, p.c);
     const int k0 = cw * kColsQ;                        // first key column (in the tile)
+    int gt = 0, uc = 0;
     bool ok = true;
-    for (int t = 0; t < n; ++t) {
-      // phase 1: P from S, kept in registers
-      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.s_full[0]), t & 1, sy, p))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      // keys after `keep` (in-tile) are masked: the diagonal tile, or keys past L
-      const bool masked = p.causal ? (t == i) : (p.L - t * kT < kT);
-      const int keep = p.causal ? r : p.L - 1 - t * kT;
-      float pr[kColsQ];
-      if (masked) p_from_s<true>(lane_base + cS + k0, c2, nl2, k0, keep, pr);
-      else p_from_s<false>(lane_base + cS + k0, c2, nl2, k0, keep, pr);
-      tc_fence_before_sync();
-      mbar_arrive(smem_addr(&sy.p_full[0]));
-      // phase 2: dP read out (its columns are then free for the next tile),
-      // dS = P * (dP - D) into the dS columns once dQ(t-1) has read them
-      if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.dp_full), t & 1, sy, p))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      uint32_t dk[kColsQ / 2];
-#pragma unroll
-      for (int c = 0; c < kColsQ / 32; ++c) {
-        uint32_t dpv[32];
-        tmem_ld32(lane_base + cP + k0 + 32 * c, dpv);
-        tmem_wait_ld(dpv);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const uint64_t dd = fadd2(
-              f32x2_pack(__uint_as_float(dpv[2 * e]), __uint_as_float(dpv[2 * e + 1])), nd2);
-          float d0, d1;
-          f32x2_unpack(fmul2(f32x2_pack(pr[32 * c + 2 * e], pr[32 * c + 2 * e + 1]), dd), d0, d1);
-          dk[16 * c + e] = pack_bf16x2(d0, d1);
-        }
-      }
-      tc_fence_before_sync();
-      mbar_arrive(smem_addr(&sy.dp_free));
-      if (t > 0 && !__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.dq_done), (t - 1) & 1, sy, p))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-#pragma unroll
-      for (int c = 0; c < kColsQ / 32; ++c)
-        tmem_st16(lane_base + cDS + k0 / 2 + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(dk + 16 * c));
+    for (int rr = 0; rr * G < units && ok; ++rr) {
+      const int u = dq_snake(rr);
+      if (u >= units) continue;
+      const DqUnit x = dq_unit(u, p);
+      const int i = x.i, n = x.n;
+      const int row = i * kT + r;
+      const size_t qoff = ((static_cast<size_t>(x.b) * p.L + row) * p.n_q + x.h) * D;
+      // Q_i becomes the A operand of S in TMEM (first warpgroup); the previous
+      // unit's products are all done (its epilogue waited for them)
+      if (cw == 0) row_to_tmem<D>(lane_base + cQ, q_rows + qoff, row < p.L);
       tmem_wait_st();
       tc_fence_before_sync();
-      mbar_arrive(smem_addr(&sy.ds_full));
-    }
-    if (ok && __all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.done), 0, sy, p))) {
+      mbar_arrive(smem_addr(&sy.a_ready));
+      const size_t srow = (static_cast<size_t>(x.b) * p.n_q + x.h) * (p.T * kT) + row;
+      const float nl = p.nlse2[srow], nd = p.nrowdot[srow];
+      const uint64_t nl2 = f32x2_pack(nl, nl), nd2 = f32x2_pack(nd, nd);
+      for (int t = 0; t < n; ++t) {
+        // phase 1: P from S, kept in registers
+        if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.s_full[0]), (gt + t) & 1, sy, p))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        // keys after `keep` (in-tile) are masked: the diagonal tile, or keys past L
+        const bool masked = p.causal ? (t == i) : (p.L - t * kT < kT);
+        const int keep = p.causal ? r : p.L - 1 - t * kT;
+        float pr[kColsQ];
+        if (masked) p_from_s<true>(lane_base + cS + k0, c2, nl2, k0, keep, pr);
+        else p_from_s<false>(lane_base + cS + k0, c2, nl2, k0, keep, pr);
+        tc_fence_before_sync();
+        mbar_arrive(smem_addr(&sy.p_full[0]));
+        // phase 2: dP read out (its columns are then free for the next tile),
+        // dS = P * (dP - D) into the dS columns once dQ(t-1) has read them
+        if (!__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.dp_full), (gt + t) & 1, sy, p))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        uint32_t dk[kColsQ / 2];
+#pragma unroll
+        for (int c = 0; c < kColsQ / 32; ++c) {
+          uint32_t dpv[32];
+          tmem_ld32(lane_base + cP + k0 + 32 * c, dpv);
+          tmem_wait_ld(dpv);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const uint64_t dd = fadd2(
+                f32x2_pack(__uint_as_float(dpv[2 * e]), __uint_as_float(dpv[2 * e + 1])), nd2);
+            float d0, d1;
+            f32x2_unpack(fmul2(f32x2_pack(pr[32 * c + 2 * e], pr[32 * c + 2 * e + 1]), dd), d0, d1);
+            dk[16 * c + e] = pack_bf16x2(d0, d1);
+          }
+        }
+        tc_fence_before_sync();
+        mbar_arrive(smem_addr(&sy.dp_free));
+        if (t > 0 && !__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.dq_done), (gt + t - 1) & 1, sy, p))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int c = 0; c < kColsQ / 32; ++c)
+          tmem_st16(lane_base + cDS + k0 / 2 + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(dk + 16 * c));
+        tmem_wait_st();
+        tc_fence_before_sync();
+        mbar_arrive(smem_addr(&sy.ds_full));
+      }
+      if (!ok || !__all_sync(0xffffffffu, wait_bounded(smem_addr(&sy.done), uc & 1, sy, p))) break;
       tc_fence_after_sync();
       constexpr int kPer = (D / 32) / kComputeWGs;    // chunks of 32 dQ columns per warpgroup
 #pragma unroll 1
       for (int q = cw * kPer; q < (cw + 1) * kPer; ++q)
         store_chunk(lane_base + cDQ + 32 * q, p.dq + qoff + 32 * q, p.scale, row < p.L);
+      gt += n;
+      ++uc;
     }
   }
   teardown(sy, p, false);
@@ -867,9 +939,8 @@ attn_status_t bwd_device_ready(cudaStream_t stream, int** status) {
   return ATTN_OK;
 }
 
-// dQ is launched as the dK/dV kernel's programmatic dependent: it reads only
-// the inputs and the row statistics (complete before dK/dV started), so it
-// needs no grid-dependency wait and fills the SMs that dK/dV's last CTAs free.
+// dK/dV is launched as the row kernel's programmatic dependent: its CTAs set
+// up while the row kernel finishes and wait for it before reading anything.
 template <int D>
 cudaError_t launch_dkdv(unsigned grid, cudaStream_t stream, const CUtensorMap& mq,
                         const CUtensorMap& mdo, const CUtensorMap& mk, const CUtensorMap& mv,
@@ -887,6 +958,10 @@ cudaError_t launch_dkdv(unsigned grid, cudaStream_t stream, const CUtensorMap& m
   return cudaLaunchKernelEx(&cfg, dkdv_kernel<D>, mq, mdo, mk, mv, p);
 }
 
+// dQ is launched as the dK/dV kernel's programmatic dependent: it reads only
+// the inputs and the row statistics (complete once dK/dV's CTAs are past their
+// wait, which is when they let dQ launch), so it needs no grid-dependency wait
+// and its persistent CTAs take the SMs that dK/dV's last CTAs free.
 template <int D>
 cudaError_t launch_dq(unsigned grid, cudaStream_t stream, const CUtensorMap& mk,
                       const CUtensorMap& mv, const CUtensorMap& mdo, const uint16_t* qh,
@@ -978,6 +1053,7 @@ attn_status_t attn_prefill_bwd(const void* q, const void* k, const void* v, cons
   p.dk = static_cast<uint16_t*>(dk);
   p.dv = static_cast<uint16_t*>(dv);
   p.status = status;
+  p.q_units = static_cast<int>(B * n_q * T);
 
   const int64_t rows = B * n_q * T * kT;
   constexpr int kRowdotRowsPerBlock = 8 * kRowdotRowsPerWarp;   // 256 threads
@@ -992,19 +1068,19 @@ attn_status_t attn_prefill_bwd(const void* q, const void* k, const void* v, cons
   const uint16_t* doh = static_cast<const uint16_t*>(dout);
   const int Lp = static_cast<int>(T * kT);
   const unsigned kv_tiles = static_cast<unsigned>(B * n_kv * T);
-  const unsigned q_tiles = static_cast<unsigned>(B * n_q * T);
+  const unsigned dq_grid = static_cast<unsigned>(B * n_q * T < sms ? B * n_q * T : sms);
   if (d_h == 128) {
     rowdot_kernel<128><<<row_blocks, 256, 0, stream>>>(oh, doh, lse, nlse2, nrowdot,
                                                        static_cast<int>(B), p.L, n_q, Lp);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     if (launch_dkdv<128>(kv_tiles, stream, mq, mdo, mk, mv, p) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (launch_dq<128>(q_tiles, stream, mk, mv, mdo, qh, p) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (launch_dq<128>(dq_grid, stream, mk, mv, mdo, qh, p) != cudaSuccess) return ATTN_ERR_CUDA;
   } else {
     rowdot_kernel<64><<<row_blocks, 256, 0, stream>>>(oh, doh, lse, nlse2, nrowdot,
                                                       static_cast<int>(B), p.L, n_q, Lp);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     if (launch_dkdv<64>(kv_tiles, stream, mq, mdo, mk, mv, p) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (launch_dq<64>(q_tiles, stream, mk, mv, mdo, qh, p) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (launch_dq<64>(dq_grid, stream, mk, mv, mdo, qh, p) != cudaSuccess) return ATTN_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
