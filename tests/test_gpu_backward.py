@@ -78,6 +78,7 @@ SHAPES = [
     (1, 257, 6, 6, True),        # MHA, one-row tail
     (1, 333, 4, 1, False),       # full attention, MQA, ragged
     (1, 1000, 8, 1, True),       # GQA-8 (one K/V head collects 8 query heads)
+    (6, 200, 4, 1, True),        # many short sequences, ragged second tile
 ]
 
 

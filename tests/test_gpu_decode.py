@@ -43,6 +43,8 @@ DECODE = [
     (2, 20000, 6, 3),      # 942 tiles over 152 CTAs: ranges cross head boundaries
     (1, 3000, 12, 1),      # g = 12
     (2, 1500, 32, 2),      # g = 16
+    (64, 100, 16, 1),      # 64 sequences of one partial tile each: 64 CTAs, g = 16
+    (40, 3000, 8, 8),      # g = 1, many sequences
 ]
 
 

@@ -50,6 +50,10 @@ SMALL = [
     (1, 1000, 2, 2, 64, False),
     (1, 128, 2, 2, 128, False),
     (1, 1, 2, 1, 64, False),
+    (48, 200, 8, 2, 128, True),     # many short sequences (B = 48), ragged second tile
+    (2, 300, 64, 1, 128, True),     # g = 64: one K/V head for 64 query heads
+    (5, 257, 10, 5, 64, True),      # g = 2, d_h = 64, one-row tail
+    (16, 128, 4, 1, 64, False),     # full attention over many batches
 ]
 
 
