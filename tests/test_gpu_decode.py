@@ -102,6 +102,15 @@ def test_decode_back_to_back_calls():
         check_full(q, k, v, o, lse, what=f"call {i}")
 
 
+def test_decode_million_token_cache():
+    """One new token against 1,000,003 cached keys (a ragged last tile; 7,813
+    key tiles per K/V head spread over every CTA)."""
+    w = W.custom(1, 1, 8, 1, 128, Lk=1_000_003)
+    q, k, v = W.make_inputs(w, "cuda", seed=1000003)
+    o, lse = _decode(q, k, v)
+    check_full(q, k, v, o, lse, what="Lk=1000003")
+
+
 @pytest.mark.parametrize("num", [10, 11])
 def test_decode_workloads(num):
     w = W.WORKLOADS[num]
