@@ -884,6 +884,11 @@ dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUten
     }
   }
   teardown(sy, p, false);
+  // This grid started while dK/dV still ran (it reads nothing dK/dV writes);
+  // it ends only once dK/dV has ended (one waiting thread keeps the CTA
+  // alive; every thread waiting cost 1.4 %), so that a programmatic dependent
+  // of this grid (the stream's next kernel) finds dK and dV complete as well.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // --------------------------------------------------------------------- host

@@ -153,6 +153,14 @@ attn_status_t attn_prefill_fwd_fp8(const void* q, const void* k, const void* v,
  *   n_q / n_kv <= 16 and d_h = 128 (ATTN_ERR_UNSUPPORTED otherwise); a NULL
  *   or too-small workspace is ATTN_ERR_INVALID_ARG. Everything else as
  *   attn_prefill_fwd.
+ *
+ * Both kernels are launched as programmatic dependents (CUDA programmatic
+ * dependent launch) of the kernel before them on `stream`: they may start
+ * their set-up while that kernel finishes, but each waits for it to complete
+ * before touching global memory, so stream order holds for every input and
+ * for the workspace. The merge kernel lets the next kernel on the stream
+ * start its own set-up early in the same way; a kernel launched without that
+ * attribute waits for the call's completion as usual.
  */
 int64_t attn_decode_workspace_bytes(int64_t B, int64_t Lk, int32_t n_q, int32_t n_kv,
                                     int32_t d_h);   /* -1 on invalid or unsupported sizes */
@@ -185,6 +193,14 @@ attn_status_t attn_decode_fwd(const void* q, const void* k, const void* v, void*
  *                     entry ignored, on exit unspecified
  *   d_h must be 64 or 128 (ATTN_ERR_UNSUPPORTED otherwise); square problems only
  *   (the forward's Lq = Lk = L). Everything else as attn_prefill_fwd.
+ *
+ * Launches: a row kernel, then the dK/dV kernel as its programmatic
+ * dependent (set-up overlaps the row kernel's end; it waits for it before
+ * reading), then the dQ kernel as dK/dV's programmatic dependent (it reads
+ * only the inputs and the row statistics, so it starts on the SMs dK/dV's
+ * last CTAs free; it does not end before dK/dV has). Every result is complete
+ * when the call's last kernel is, for stream-ordered and programmatic
+ * successors alike.
  */
 int64_t attn_prefill_bwd_workspace_bytes(int64_t B, int64_t L, int32_t n_q, int32_t n_kv,
                                          int32_t d_h);   /* -1 on invalid or unsupported sizes */

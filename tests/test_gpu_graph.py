@@ -183,3 +183,27 @@ def test_concurrent_streams_match_sequential_calls():
     for got, want in zip(par, seq):
         for g, w in zip(got, want):
             assert torch.equal(g, w)
+
+
+def test_programmatic_successor_sees_complete_backward_outputs():
+    """A kernel launched as a programmatic dependent right after the backward
+    must find dK and dV complete. The shape makes the dQ kernel (the call's
+    last) short and dK/dV long (full attention, 64 query heads on one K/V
+    head: 8 dK/dV CTAs of 512 steps against ~3 dQ units per CTA). The decode
+    step, whose kernels are programmatic dependents, reads dK and dV as its
+    cache straight after the backward; it must equal the same decode step run
+    after a synchronize."""
+    w = W.custom(1, 1024, 64, 1, 128, causal=False)
+    q, k, v = W.make_inputs(w, "cuda", seed=51)
+    do = W.make_grad(w, "cuda", seed=51)
+    o, lse = attn_prefill(q, k, v, causal=False)
+    g = torch.Generator(device="cuda").manual_seed(52)
+    qd = torch.randn(1, 1, 16, 128, device="cuda", generator=g).to(torch.bfloat16)
+    torch.cuda.synchronize()
+    dq, dk, dv = attn_prefill_backward(q, k, v, o, lse, do, causal=False)
+    od, ld = attn_decode(qd, dk, dv)                 # no host sync in between
+    torch.cuda.synchronize()
+    assert attn_device_check() == ATTN_OK
+    od2, ld2 = attn_decode(qd, dk, dv)
+    torch.cuda.synchronize()
+    assert torch.equal(od, od2) and torch.equal(ld, ld2)
