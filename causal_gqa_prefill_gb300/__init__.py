@@ -12,7 +12,8 @@ from .api import (AttnError, attn_decode, attn_decode_fwd, attn_decode_workspace
                   attn_prefill, attn_prefill_fp8, attn_prefill_fwd, attn_prefill_fwd_chunk,
                   attn_prefill_fwd_fp8, attn_device_check, attn_prefill_grid_size,
                   attn_prefill_backward, attn_prefill_bwd, attn_prefill_bwd_workspace_bytes,
-                  attn_selftest_wait_timeout, attn_prefill_fwd_host,
+                  attn_selftest_wait_timeout, attn_selftest_wait_timeout_noalloc,
+                  attn_prefill_fwd_host,
                   attn_prefill_host_staging_bytes)
 
 __all__ = [
@@ -21,6 +22,6 @@ __all__ = [
     "attn_prefill_fp8", "attn_prefill_fwd_fp8", "attn_decode", "attn_decode_fwd",
     "attn_decode_workspace_bytes", "attn_device_check", "attn_prefill_backward",
     "attn_prefill_bwd", "attn_prefill_bwd_workspace_bytes", "attn_selftest_wait_timeout",
-    "attn_prefill_fwd_host", "attn_prefill_host_staging_bytes",
+    "attn_selftest_wait_timeout_noalloc", "attn_prefill_fwd_host", "attn_prefill_host_staging_bytes",
     "attn_prefill_grid_size", "load_library", "library_path", "status_string",
 ]

@@ -60,6 +60,7 @@ _SIGNATURES = {
                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                         ctypes.c_float, ctypes.c_void_p]),
     "attn_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p]),
+    "attn_selftest_wait_timeout_noalloc": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p]),
     "attn_prefill_host_staging_bytes": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int64,
                                                          ctypes.c_int64, ctypes.c_int32,
                                                          ctypes.c_int32, ctypes.c_int32]),

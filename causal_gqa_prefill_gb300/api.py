@@ -232,6 +232,13 @@ def attn_selftest_wait_timeout(spin_cycles: int, stream=None) -> int:
     return int(_abi.load().attn_selftest_wait_timeout(int(spin_cycles), _stream_handle(stream)))
 
 
+def attn_selftest_wait_timeout_noalloc(spin_cycles: int, stream=None) -> int:
+    """The wait-limit diagnostic reporting into the allocation-free entry
+    point's fixed status word (raw status of the launch)."""
+    return int(_abi.load().attn_selftest_wait_timeout_noalloc(int(spin_cycles),
+                                                             _stream_handle(stream)))
+
+
 def attn_prefill_grid_size(B, L, n_q, n_kv, d_h, causal=True) -> int:
     return int(_abi.load().attn_prefill_grid_size(int(B), int(L), int(n_q), int(n_kv), int(d_h),
                                                   int(bool(causal))))

@@ -9,6 +9,15 @@
 
 #include "attn_prefill.h"
 
+namespace gb300_host {
+// attn_prefill.cu: every check of attn_prefill_fwd_chunk short of the launch,
+// including the device's first-call set-up.
+attn_status_t forward_preflight(const void* q, const void* k, const void* v, const void* o,
+                                const float* lse, int64_t B, int64_t Lq, int64_t Lk,
+                                int32_t n_q, int32_t n_kv, int32_t d_h, int32_t causal,
+                                float scale, cudaStream_t stream);
+}  // namespace gb300_host
+
 namespace {
 
 constexpr int64_t kAlign = 256;
@@ -67,6 +76,13 @@ attn_status_t attn_prefill_fwd_host(const void* q, const void* k, const void* v,
   const size_t qb = static_cast<size_t>(B * Lq * n_q * d_h * 2);
   const size_t kvb = static_cast<size_t>(B * Lk * n_kv * d_h * 2);
   const size_t lb = static_cast<size_t>(B * n_q * Lq * 4);
+  // Everything the forward could refuse (sizes, the device, a first call
+  // during capture) is settled before the first copy is enqueued, so an error
+  // return leaves nothing half done on the stream.
+  const attn_status_t pre = gb300_host::forward_preflight(
+      base + s.q, base + s.k, base + s.v, base + s.o, reinterpret_cast<float*>(base + s.lse), B,
+      Lq, Lk, n_q, n_kv, d_h, causal, scale, stream);
+  if (pre != ATTN_OK) return pre;
   // one copy per tensor, in, then the forward, then one copy per result, out
   if (cudaMemcpyAsync(base + s.q, q, qb, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
       cudaMemcpyAsync(base + s.k, k, kvb, cudaMemcpyHostToDevice, stream) != cudaSuccess ||

@@ -439,10 +439,14 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem,
     const int u = snake_unit(rr);
     if (u >= p.units) continue;
     const Unit x = decode_unit(u, p);
-    const int n = x.n[slot];
+    // this warpgroup's query tile (selected, not indexed: a runtime index
+    // would put the unit in local memory)
+    const int n = slot ? x.n[1] : x.n[0];
     if (n == 0) continue;
-    const int row = x.qtile[slot] * kBM + r;                    // chunk row
-    const int qrow0 = p.offset + x.qtile[slot] * kBM;           // absolute position of row 0
+    const int qtile = slot ? x.qtile[1] : x.qtile[0];
+    const int head = slot ? x.head[1] : x.head[0];
+    const int row = qtile * kBM + r;                            // chunk row
+    const int qrow0 = p.offset + qtile * kBM;                   // absolute position of row 0
     float m_run = -INFINITY, l_run = 0.0f;
     for (int j = 0; j < n; ++j) {
       if (!__all_sync(0xffffffffu, wait_phase(bar_s, ph_s, ctl, p))) return;
@@ -562,9 +566,9 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem,
     // each store to global memory covers four whole rows' 128-byte pieces
     // (eight threads per row) instead of 32 scattered 16-byte pieces.
     const uint32_t stg = o_stage + warp * kOStageWarpBytes;
-    const int row0 = x.qtile[slot] * kBM + (warp & 3) * 32;    // first row of this warp
+    const int row0 = qtile * kBM + (warp & 3) * 32;             // first row of this warp
     const size_t hstride = static_cast<size_t>(p.n_q) * D;     // elements between rows
-    uint16_t* obase = p.o + (static_cast<size_t>(x.b) * p.Lq * p.n_q + x.head[slot]) *
+    uint16_t* obase = p.o + (static_cast<size_t>(x.b) * p.Lq * p.n_q + head) *
                                 static_cast<size_t>(D);
 #pragma unroll 1
     for (int hh = 0; hh < D / 64; ++hh) {
@@ -594,7 +598,7 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem,
     }
     if (valid) {
       const float m_fin = (m_run == -INFINITY) ? 0.0f : m_run;
-      p.lse[(static_cast<size_t>(x.b) * p.n_q + x.head[slot]) * p.Lq + row] =
+      p.lse[(static_cast<size_t>(x.b) * p.n_q + head) * p.Lq + row] =
           (m_fin + log2f(l_run)) * 0.69314718055994530942f;
     }
   }
@@ -867,6 +871,93 @@ attn_status_t launch_forward(const void* q, const void* k, const void* v, void* 
 
 }  // namespace
 
+// ----------------------------------------------------- allocation-free variant
+//
+// For callers that cannot allocate device memory: code running inside a
+// memory pool or arena that must own every allocation (a cudaMalloc behind
+// its back escapes its accounting and limits), or a host framework that
+// forbids the library from touching the allocator. The only global memory the
+// kernel needs beyond its inputs and outputs is its status word; here that
+// word lives in the fixed array below, part of the library's own device image
+// (zero when the library is loaded; the kernel only sets bits in it, and
+// attn_device_check reads and clears it).
+
+constexpr size_t kNoAllocScratchBytes = 256;            // stated maximum scratch
+constexpr size_t kNoAllocScratchNeeded = sizeof(int);   // one status word, any problem size
+static_assert(kNoAllocScratchNeeded <= kNoAllocScratchBytes,
+              "the allocation-free variant's scratch exceeds its fixed array");
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+struct NoAllocState {
+  bool ready = false;
+  int sms = 0;
+  int* scratch = nullptr;    // device address of g_noalloc_scratch on this device
+};
+
+NoAllocState g_noalloc[kMaxDevices];
+
+// Once per device, with that device current: resolve the device address of
+// the static scratch array (the host-side symbol is only a stand-in and must
+// never be handed to a kernel), query the device, set the kernels'
+// shared-memory limit and resolve the tensor-map encoder. Nothing here
+// allocates. Like the allocating path's set-up, a first call made while
+// `stream` is being captured is refused (ATTN_ERR_UNSUPPORTED) and sets up
+// nothing: the module look-ups it makes are not stream work and have no place
+// in a graph.
+attn_status_t noalloc_state(cudaStream_t stream, NoAllocState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  NoAllocState& st = g_noalloc[dev];
+  if (!st.ready) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+      cudaGetLastError();
+      return ATTN_ERR_UNSUPPORTED;
+    }
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;
+    if (!configure_kernels()) return ATTN_ERR_UNSUPPORTED;
+    if (!g_encode) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return ATTN_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    void* scratch = nullptr;
+    if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || scratch == nullptr)
+      return ATTN_ERR_CUDA;
+    st.sms = sms;
+    st.scratch = static_cast<int*>(scratch);
+    st.ready = true;
+  }
+  *out = &st;
+  return ATTN_OK;
+}
+
+// Reads a status word (synchronously) and clears it when set; *word gets its
+// value. Allocates nothing.
+attn_status_t read_and_clear(int* status, int* word) {
+  *word = 0;
+  if (cudaMemcpy(word, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (*word != 0 && cudaMemset(status, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+}  // namespace
+
 // The per-device status word (allocated on first use) for the other kernels of
 // this library, so that attn_device_check reports their timeouts as well.
 namespace gb300_host {
@@ -876,6 +967,19 @@ attn_status_t device_status_word(cudaStream_t stream, int** status) {
   if (ds != ATTN_OK) return ds;
   *status = st->status;
   return ATTN_OK;
+}
+
+// Every check attn_prefill_fwd_chunk makes before it launches (arguments,
+// sizes, the device and the first-call set-up), without launching: the host
+// entry point runs it on its staging pointers before enqueueing any copy.
+attn_status_t forward_preflight(const void* q, const void* k, const void* v, const void* o,
+                                const float* lse, int64_t B, int64_t Lq, int64_t Lk,
+                                int32_t n_q, int32_t n_kv, int32_t d_h, int32_t causal,
+                                float scale, cudaStream_t stream) {
+  const attn_status_t bad = validate(q, k, v, o, lse, B, Lq, Lk, n_q, n_kv, d_h, causal, scale);
+  if (bad != ATTN_OK) return bad;
+  DeviceState* st = nullptr;
+  return device_state(stream, &st);
 }
 }  // namespace gb300_host
 
@@ -939,17 +1043,18 @@ attn_status_t attn_device_check(void* stream_ptr) {
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
   int* status = nullptr;
+  int* noalloc_status = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_dev[dev].ready) return ATTN_OK;
-    status = g_dev[dev].status;
+    if (g_dev[dev].ready) status = g_dev[dev].status;
+    if (g_noalloc[dev].ready) noalloc_status = g_noalloc[dev].scratch;
   }
-  int word = 0;
-  if (cudaMemcpy(&word, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+  // the allocating entry points' word, then the allocation-free variant's
+  int word = 0, noalloc_word = 0;
+  if (status && read_and_clear(status, &word) != ATTN_OK) return ATTN_ERR_CUDA;
+  if (noalloc_status && read_and_clear(noalloc_status, &noalloc_word) != ATTN_OK)
     return ATTN_ERR_CUDA;
-  if (word == 0) return ATTN_OK;
-  if (cudaMemset(status, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
-  return ATTN_ERR_TIMEOUT;
+  return (word | noalloc_word) == 0 ? ATTN_OK : ATTN_ERR_TIMEOUT;
 }
 
 attn_status_t attn_selftest_wait_timeout(int64_t spin_cycles, void* stream_ptr) {
@@ -981,70 +1086,7 @@ int64_t attn_prefill_grid_size(int64_t B, int64_t L, int32_t n_q, int32_t n_kv, 
 
 }  // extern "C"
 
-// ----------------------------------------------------- allocation-free variant
-//
-// For callers that cannot allocate device memory: code running inside a
-// memory pool or arena that must own every allocation (a cudaMalloc behind
-// its back escapes its accounting and limits), or a host framework that
-// forbids the library from touching the allocator. The only global memory the kernel
-// needs beyond its inputs and outputs is its status word; here that word
-// lives in the fixed array below, part of the library's own device image.
-
-constexpr size_t kNoAllocScratchBytes = 256;       // stated maximum scratch
-constexpr size_t kNoAllocScratchNeeded = sizeof(int);   // one status word, any problem size
-
-static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
-
-namespace {
-
-struct NoAllocState {
-  bool ready = false;
-  int sms = 0;
-  int* scratch = nullptr;    // device address of g_noalloc_scratch on this device
-};
-
-NoAllocState g_noalloc[kMaxDevices];
-
-// Once per device, with that device current: resolve the device address of
-// the static scratch array (the host-side symbol is only a stand-in and must
-// never be handed to a kernel), query the device, set the kernels'
-// shared-memory limit and resolve the tensor-map encoder. Nothing here
-// allocates.
-attn_status_t noalloc_state(NoAllocState** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  NoAllocState& st = g_noalloc[dev];
-  if (!st.ready) {
-    int major = 0, minor = 0, sms = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return ATTN_ERR_CUDA;
-    if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;
-    if (!configure_kernels()) return ATTN_ERR_UNSUPPORTED;
-    if (!g_encode) {
-      cudaDriverEntryPointQueryResult q;
-      void* fn = nullptr;
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                           cudaEnableDefault, &q) != cudaSuccess ||
-          q != cudaDriverEntryPointSuccess || fn == nullptr)
-        return ATTN_ERR_CUDA;
-      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
-    }
-    void* scratch = nullptr;
-    if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || scratch == nullptr)
-      return ATTN_ERR_CUDA;
-    st.sms = sms;
-    st.scratch = static_cast<int*>(scratch);
-    st.ready = true;
-  }
-  *out = &st;
-  return ATTN_OK;
-}
-
-}  // namespace
+// ------------------------------------------ allocation-free entry points
 
 extern "C" attn_status_t attn_prefill_fwd_noalloc(const void* q, const void* k, const void* v,
                                                   void* o, float* lse, int64_t B, int64_t L,
@@ -1052,15 +1094,26 @@ extern "C" attn_status_t attn_prefill_fwd_noalloc(const void* q, const void* k, 
                                                   int32_t causal, float scale, void* stream_ptr) {
   const attn_status_t bad = validate(q, k, v, o, lse, B, L, L, n_q, n_kv, d_h, causal, scale);
   if (bad != ATTN_OK) return bad;
-  if (kNoAllocScratchNeeded > kNoAllocScratchBytes) return ATTN_ERR_UNSUPPORTED;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   NoAllocState* st = nullptr;
-  const attn_status_t ds = noalloc_state(&st);
+  const attn_status_t ds = noalloc_state(stream, &st);
   if (ds != ATTN_OK) return ds;
-  // The status word must start at zero for every call (the kernel only ORs
-  // error bits into it).
-  if (cudaMemsetAsync(st->scratch, 0, kNoAllocScratchNeeded, stream) != cudaSuccess)
-    return ATTN_ERR_CUDA;
+  // The status word is not cleared here: like the allocating path's word it
+  // collects every wait timeout since attn_device_check last read it.
   return launch_forward(q, k, v, o, lse, B, L, L, n_q, n_kv, d_h, causal, scale, stream,
                         st->scratch, st->sms);
+}
+
+extern "C" attn_status_t attn_selftest_wait_timeout_noalloc(int64_t spin_cycles,
+                                                            void* stream_ptr) {
+  if (spin_cycles < 1 || spin_cycles > kSpinLimitCycles) return ATTN_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  NoAllocState* st = nullptr;
+  const attn_status_t ds = noalloc_state(stream, &st);
+  if (ds != ATTN_OK) return ds;
+  Params p{};
+  p.status = st->scratch;
+  p.spin_limit = spin_cycles;
+  wait_selftest_kernel<<<1, 64, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

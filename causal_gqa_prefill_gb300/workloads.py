@@ -166,21 +166,27 @@ def custom(B, L, n_q, n_kv, d_h, causal=True, number=0, name=None, Lk=0,
 def sampled_rows(w: Workload, count: int = 4096, tile: int = 128):
     """Rows (b, h, i) to check on large workloads.
 
-    For s = 0..count-1: position in tile = s mod 128 and head =
-    (s + s div 128) mod n_q, so every head and every intra-tile position is
-    covered and heads meet many positions; query tile and batch index are
-    drawn from numpy's default_rng(seed) uniformly. Rows 0 and L-1 of every
-    (b, head) are added. Returns a sorted, de-duplicated int64 array [R, 3].
+    For s = 0..count-1: position in tile = s mod 128, head =
+    (s + 7 (s div 128)) mod n_q and query tile = perm[(s + s div T) mod T],
+    perm a permutation of the T tiles drawn from numpy's default_rng(seed).
+    So every head and every intra-tile position is covered, every tile is hit
+    whenever count >= T (the tail tile's positions past L-1 fall on row L-1),
+    and the shifts by s div 128 and s div T keep head, tile and position from
+    locking together when T and n_q share factors with 128 (each tile meets
+    several heads and positions). The batch index is drawn from the same
+    generator. Rows 0 and L-1 of every (b, head) are added.
+    Returns a sorted, de-duplicated int64 array [R, 3].
     """
     import numpy as np
 
     T = (w.L + tile - 1) // tile
     rng = np.random.default_rng(w.seed)
     s = np.arange(count, dtype=np.int64)
-    i = rng.integers(0, T, count) * tile + (s % tile)
+    perm = rng.permutation(T).astype(np.int64)
+    i = perm[(s + s // T) % T] * tile + (s % tile)
     i = np.minimum(i, w.L - 1)
     b = rng.integers(0, w.B, count)
-    rows = [np.stack([b, (s + s // tile) % w.n_q, i], axis=1)]
+    rows = [np.stack([b, (s + 7 * (s // tile)) % w.n_q, i], axis=1)]
     for bb in range(w.B):
         for h in range(w.n_q):
             rows.append(np.array([[bb, h, 0], [bb, h, w.L - 1]], dtype=np.int64))

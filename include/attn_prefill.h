@@ -45,8 +45,9 @@
  * stream it is given (attn_decode_fwd as two kernel nodes joined by a
  * programmatic dependency); replaying the graph recomputes from whatever the
  * captured input buffers hold then. attn_device_check synchronizes and cannot
- * be captured; attn_prefill_fwd_host uses its own streams and is not meant
- * for capture.
+ * be captured. attn_prefill_fwd_host enqueues its copies and its launch on
+ * the caller's stream like the other entry points, but it is not covered by
+ * this library's capture tests, so nothing is promised for it under capture.
  */
 #ifndef ATTN_PREFILL_H
 #define ATTN_PREFILL_H
@@ -228,10 +229,13 @@ attn_status_t attn_prefill_bwd(const void* q, const void* k, const void* v, cons
  *                    device copies of q, k, v, o, lse; contents on entry
  *                    ignored, on exit unspecified. A call must not share a
  *                    staging buffer with another call still in flight.
- *   Returns ATTN_ERR_INVALID_ARG before enqueueing anything for NULL pointers,
- *   a misaligned or too-small staging buffer and the argument errors of
- *   attn_prefill_fwd_chunk; ATTN_ERR_UNSUPPORTED for its unsupported sizes;
- *   ATTN_ERR_CUDA if a copy cannot be enqueued.
+ *   Every check of attn_prefill_fwd_chunk (arguments, sizes, the device and
+ *   its first-call set-up) runs before the first copy is enqueued, so
+ *   ATTN_ERR_INVALID_ARG (NULL pointers, a misaligned or too-small staging
+ *   buffer, the forward's argument errors) and ATTN_ERR_UNSUPPORTED (its
+ *   unsupported sizes or device, a first call during capture) leave nothing
+ *   enqueued. ATTN_ERR_CUDA: a copy or the launch could not be enqueued
+ *   (work enqueued before it stays on the stream).
  */
 int64_t attn_prefill_host_staging_bytes(int64_t B, int64_t Lq, int64_t Lk, int32_t n_q,
                                         int32_t n_kv, int32_t d_h);  /* -1 on invalid sizes */
@@ -247,8 +251,10 @@ const char* attn_status_string(attn_status_t status);
 /*
  * Synchronises `stream`, then reports: ATTN_ERR_CUDA if the stream or an
  * earlier launch failed, ATTN_ERR_TIMEOUT if any launch on the current device
- * since the previous check hit a wait limit (the status word is then cleared),
- * else ATTN_OK.
+ * since the previous check hit a wait limit, else ATTN_OK. It reads two
+ * status words, the one the allocating entry points share and the fixed one
+ * of attn_prefill_fwd_noalloc, and clears whichever was set. It allocates
+ * nothing.
  */
 attn_status_t attn_device_check(void* stream);
 
@@ -266,6 +272,14 @@ attn_status_t attn_device_check(void* stream);
 attn_status_t attn_selftest_wait_timeout(int64_t spin_cycles, void* stream);
 
 /*
+ * The same diagnostic for the allocation-free entry point: the wait's status
+ * lands in attn_prefill_fwd_noalloc's fixed status word, which the next
+ * attn_device_check reports and clears. Allocates nothing; its first call on
+ * a device does attn_prefill_fwd_noalloc's set-up (refused during capture).
+ */
+attn_status_t attn_selftest_wait_timeout_noalloc(int64_t spin_cycles, void* stream);
+
+/*
  * Number of persistent CTAs the forward kernel launches for these sizes on
  * the current device (min(#SMs, #work units)), or -1 on an argument error.
  * Host-side only apart from the SM-count query; used for reporting.
@@ -281,22 +295,25 @@ int64_t attn_prefill_grid_size(int64_t B, int64_t L, int32_t n_q, int32_t n_kv,
  * callers that cannot let a library allocate device memory: code whose
  * device memory all comes from its own pool or arena (a cudaMalloc behind
  * its back would escape its accounting and limits), or a host framework
- * that owns the allocator and forbids libraries to call it. The one piece of global scratch the kernel uses
- * (its 4-byte status word) sits in a fixed 256-byte array compiled into the
- * library instead of a cudaMalloc'd buffer; every GPU that loads the library
- * holds that array until process exit. This kernel's scratch does not grow
- * with the problem size, so every size attn_prefill_fwd accepts fits; a
- * build whose scratch exceeded the 256 bytes would return
- * ATTN_ERR_UNSUPPORTED.
+ * that owns the allocator and forbids libraries to call it. The one piece
+ * of global scratch the kernel uses (its 4-byte status word) sits in a fixed
+ * 256-byte array compiled into the library instead of a cudaMalloc'd buffer;
+ * every GPU that loads the library holds that array until process exit. This
+ * kernel's scratch does not grow with the problem size, so every size
+ * attn_prefill_fwd accepts fits (a build whose scratch exceeded the 256 bytes
+ * would fail to compile).
  *
  * The first call on a device does a one-time set-up on that device (it
  * looks up the array's device address and sets the kernels' shared-memory
- * limit, without allocating); make that first call before any stream capture.
- * Each call clears the status word on `stream` before its launch. All calls
+ * limit, without allocating); made while `stream` is being captured, that
+ * first call returns ATTN_ERR_UNSUPPORTED and sets up nothing, so make it
+ * before any stream capture. The status word is zero when the library is
+ * loaded; a wait that runs past its limit sets a bit in it, and
+ * attn_device_check reports it (ATTN_ERR_TIMEOUT, outputs of that launch
+ * undefined) and clears it, as for the allocating entry points. All calls
  * share the one array: calls that overlap on the GPU (different streams, no
- * ordering between them) race on it. A wait that runs past its limit in this
- * variant is recorded only in that array; attn_device_check does not report
- * it.
+ * ordering between them) race on it, and a timeout is then not tied to one
+ * call.
  */
 attn_status_t attn_prefill_fwd_noalloc(const void* q, const void* k, const void* v,
                                        void* o, float* lse,

@@ -134,7 +134,6 @@ def attention_rows(q, k, v, rows, *, causal: bool = True, scale: float | None = 
         raise ValueError("negative row index")
     if rows.size and ((rows[:, 0] >= B).any() or (rows[:, 1] >= n_q).any() or (rows[:, 2] >= L).any()):
         raise ValueError("row index out of range")
-    g = n_q // n_kv
     out_o = np.zeros((rows.shape[0], d), dtype=np.float64)
     out_lse = np.zeros(rows.shape[0], dtype=np.float64)
     # Group the requested rows by (b, h); each group shares one K/V head.
@@ -145,7 +144,7 @@ def attention_rows(q, k, v, rows, *, causal: bool = True, scale: float | None = 
         if grp.size == 0:
             continue
         b, h = int(srt[grp[0], 0]), int(srt[grp[0], 1])
-        kvh = h // g
+        kvh = kv_head_of(h, n_q, n_kv)
         kmat = np.asarray(k[b, :, kvh, :], dtype=np.float64)
         vmat = np.asarray(v[b, :, kvh, :], dtype=np.float64)
         idx = srt[grp, 2]
@@ -177,13 +176,12 @@ def attention(q, k, v, *, causal: bool = True, scale: float | None = None):
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     scale = float(scale)
-    g = n_q // n_kv
     o = np.zeros((B, L, n_q, d), dtype=np.float64)
     lse = np.zeros((B, n_q, L), dtype=np.float64)
     step = max(1, min(256, _MAX_SCORE_ELEMS // max(Lk, 1)))
     for b in range(B):
         for h in range(n_q):
-            kvh = h // g
+            kvh = kv_head_of(h, n_q, n_kv)
             kmat = np.asarray(k[b, :, kvh, :], dtype=np.float64)
             vmat = np.asarray(v[b, :, kvh, :], dtype=np.float64)
             for i0 in range(0, L, step):

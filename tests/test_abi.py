@@ -177,6 +177,8 @@ def test_selftest_rejects_bad_limits(lib):
     assert cg.attn_selftest_wait_timeout(0, stream=0) == cg.ATTN_ERR_INVALID_ARG
     assert cg.attn_selftest_wait_timeout(-5, stream=0) == cg.ATTN_ERR_INVALID_ARG
     assert cg.attn_selftest_wait_timeout((1 << 31) + 1, stream=0) == cg.ATTN_ERR_INVALID_ARG
+    for bad in (0, -5, (1 << 31) + 1):
+        assert cg.attn_selftest_wait_timeout_noalloc(bad, stream=0) == cg.ATTN_ERR_INVALID_ARG
 
 
 def test_chunk_workload_flops_reduce_to_square():
@@ -208,15 +210,33 @@ def test_metric_flops_match_the_oracle_cost_model():
             assert w.metric_flops() == (fwd * 5 // 2 if w.backward else fwd)
 
 
-def test_sampled_rows_cover_heads_and_tile_positions():
-    for w in (workloads.WORKLOADS[4], workloads.WORKLOADS[5]):
+def test_sampled_rows_cover_every_head_tile_and_tile_position():
+    # the sampled-row workloads (the L=32768 and L=131072 layers and the
+    # 16384-row chunk): every query tile, every head and every position inside
+    # a tile is checked, plus rows 0 and L-1 of every head
+    for num in (4, 5, 7, 8, 9):
+        w = workloads.WORKLOADS[num]
         rows = workloads.sampled_rows(w)
         assert rows.shape[1] == 3 and len(rows) >= 4000
         assert set(rows[:, 1]) == set(range(w.n_q))
         assert set(rows[:, 2] % 128) == set(range(128))
+        T = (w.L + 127) // 128
+        assert T <= 4096
+        assert set(rows[:, 2] // 128) == set(range(T)), num
         for h in range(w.n_q):
             sel = rows[rows[:, 1] == h, 2]
             assert 0 in sel and w.L - 1 in sel
         assert (rows[:, 2] < w.L).all() and (rows[:, 2] >= 0).all()
-        T = w.L // 128
-        assert len(set(rows[:, 2] // 128)) >= min(T, 200)
+        assert (rows[:, 0] == 0).all()
+        # every tile meets more than one head where there are samples to spare
+        if 4096 >= 2 * T:
+            heads_per_tile = [len(set(rows[rows[:, 2] // 128 == t, 1])) for t in range(T)]
+            assert min(heads_per_tile) >= 2, num
+
+
+def test_sampled_rows_ragged_tail_and_batches():
+    w = workloads.custom(3, 1000, 6, 2, 128)      # 8 tiles, the last one ragged
+    rows = workloads.sampled_rows(w, count=512)
+    assert set(rows[:, 2] // 128) == set(range(8))
+    assert (rows[:, 2] <= 999).all() and 999 in rows[:, 2]
+    assert set(rows[:, 0]) == {0, 1, 2} and set(rows[:, 1]) == set(range(6))

@@ -420,7 +420,7 @@ def test_long_context_shape_costs():
 
 MUTANTS = {
     "mask_excludes_diagonal": ("keys[None, :] <= pos[:, None]", "keys[None, :] < pos[:, None]"),
-    "kv_head_modulo": ("kvh = h // g", "kvh = h % n_kv"),
+    "kv_head_modulo": ("return h // (n_q // n_kv)", "return h % n_kv"),
     "scale_dropped": ("s = scale * (qrows @ krows.T)", "s = (qrows @ krows.T)"),
     "lse_without_max": ("lse = m_safe + np.log(l)", "lse = np.log(l)"),
     "no_max_subtraction": ("p = np.exp(s - m_safe[:, None])", "p = np.exp(s)"),
