@@ -75,6 +75,9 @@ constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kStatusTimeout = 1;
 constexpr long long kSpinLimitCycles = 1ll << 31;   // about a second at 2 GHz
+// Smallest batch of (b, kv-head) groups in the unit order, in rounds of the
+// persistent grid (decode_unit).
+constexpr int kBatchRounds = 8;
 
 // D = head dim; F8: Q, K, V (and P) in fp8 e4m3 instead of bf16.
 template <int D, bool F8>
@@ -108,6 +111,8 @@ struct Params {
   float o_scale;        // multiplies O / l in the epilogue (the V descale for fp8, else 1)
   int groups;           // B * n_kv
   int units;            // pairs per group * groups
+  int pairs;            // pairs (units) per group
+  int batch;            // groups per batch (see decode_unit)
   long long spin_limit;
 };
 
@@ -125,8 +130,15 @@ struct Unit {
   int head[2], qtile[2], n[2];
 };
 
-// Unit u -> (batch, K/V head, two query tiles). Units are ordered by pair
-// index first, so ascending u means descending causal length (longest first).
+// Unit u -> (batch, K/V head, two query tiles). The (b, kv-head) groups are
+// taken in batches of p.batch consecutive groups (the last batch may be
+// smaller); within a batch units are ordered by pair index first, so
+// ascending u means descending causal length (longest first) batch by batch,
+// and only one batch's K/V is streamed at a time. The host batches only when
+// the K/V of all groups exceeds 1.5 times the L2: a batch is as many groups as
+// fit half of the L2, but at least kBatchRounds rounds of the persistent
+// grid, so the snake order still balances it. Otherwise there is one batch
+// and the order is pair-major over all groups.
 // Query row i of the chunk sits at absolute position offset + i (the chunk is
 // the end of the key range; offset = 0 for square prefill).
 // Within one (b, kv-head) group the g*T query tiles are listed longest first
@@ -134,8 +146,13 @@ struct Unit {
 // slot 0 the next one, and their key-tile counts differ by at most one.
 __device__ __forceinline__ Unit decode_unit(int u, const Params& p) {
   Unit x;
-  const int pair = u / p.groups;
-  const int grp = u - pair * p.groups;
+  const int per_batch = p.batch * p.pairs;
+  const int bi = u / per_batch;
+  const int v = u - bi * per_batch;
+  const int g0 = bi * p.batch;
+  const int nb = min(p.batch, p.groups - g0);
+  const int pair = v / nb;
+  const int grp = g0 + (v - pair * nb);
   x.b = grp / p.n_kv;
   x.kvh = grp - x.b * p.n_kv;
   const int total = p.g * p.Tq;
@@ -678,6 +695,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 struct DeviceState {
   bool ready = false;
   int sms = 0;
+  int l2 = 0;              // L2 cache bytes
   int* status = nullptr;
 };
 
@@ -722,10 +740,11 @@ attn_status_t device_state(cudaStream_t stream, DeviceState** out) {
       cudaGetLastError();
       return ATTN_ERR_UNSUPPORTED;
     }
-    int major = 0, minor = 0, sms = 0;
+    int major = 0, minor = 0, sms = 0, l2 = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
       return ATTN_ERR_CUDA;
     if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;   // built for sm_103a only
     if (!configure_kernels()) return ATTN_ERR_UNSUPPORTED;
@@ -745,6 +764,7 @@ attn_status_t device_state(cudaStream_t stream, DeviceState** out) {
       return ATTN_ERR_CUDA;
     }
     st.sms = sms;
+    st.l2 = l2;
     st.status = status;
     st.ready = true;
   }
@@ -832,7 +852,8 @@ void launch_instance(int grid, cudaStream_t stream, const CUtensorMap& mq, const
 attn_status_t launch_forward(const void* q, const void* k, const void* v, void* o, float* lse,
                              int64_t B, int64_t Lq, int64_t Lk, int32_t n_q, int32_t n_kv,
                              int32_t d_h, int32_t causal, float scale, cudaStream_t stream,
-                             int* status, int sms, bool f8 = false, float qk_descale = 1.0f,
+                             int* status, int sms, int l2, bool f8 = false,
+                             float qk_descale = 1.0f,
                              float v_descale = 1.0f) {
   int Tq = 0, units = 0;
   count_units(B, Lq, Lk, n_q, n_kv, &Tq, &units);
@@ -859,6 +880,22 @@ attn_status_t launch_forward(const void* q, const void* k, const void* v, void* 
   p.scale_pos = p.c > 0.0f ? 1 : 0;
   p.groups = static_cast<int>(B * n_kv);
   p.units = units;
+  p.pairs = units / p.groups;
+  p.batch = p.groups;
+  {
+    // Batches of groups only when the K/V of all groups is well beyond the
+    // L2 (more than 1.5 times its size): then as many groups as fit half of
+    // it, but at least kBatchRounds rounds of the grid's units per batch.
+    const int64_t kv_group = 2 * Lk * static_cast<int64_t>(d_h) * (f8 ? 1 : 2);
+    if (2 * kv_group * p.groups > 3 * static_cast<int64_t>(l2)) {
+      const int64_t grid_ctas = units < sms ? units : sms;
+      const int64_t by_rounds = (kBatchRounds * grid_ctas + p.pairs - 1) / p.pairs;
+      const int64_t by_l2 = (l2 / 2) / kv_group;
+      int64_t want = by_rounds > by_l2 ? by_rounds : by_l2;
+      if (want < 1) want = 1;
+      p.batch = static_cast<int>(want < p.groups ? want : p.groups);
+    }
+  }
   p.spin_limit = kSpinLimitCycles;
 
   const int grid = units < sms ? units : sms;
@@ -894,6 +931,7 @@ namespace {
 struct NoAllocState {
   bool ready = false;
   int sms = 0;
+  int l2 = 0;
   int* scratch = nullptr;    // device address of g_noalloc_scratch on this device
 };
 
@@ -919,10 +957,11 @@ attn_status_t noalloc_state(cudaStream_t stream, NoAllocState** out) {
       cudaGetLastError();
       return ATTN_ERR_UNSUPPORTED;
     }
-    int major = 0, minor = 0, sms = 0;
+    int major = 0, minor = 0, sms = 0, l2 = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
       return ATTN_ERR_CUDA;
     if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;
     if (!configure_kernels()) return ATTN_ERR_UNSUPPORTED;
@@ -939,6 +978,7 @@ attn_status_t noalloc_state(cudaStream_t stream, NoAllocState** out) {
     if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || scratch == nullptr)
       return ATTN_ERR_CUDA;
     st.sms = sms;
+    st.l2 = l2;
     st.scratch = static_cast<int*>(scratch);
     st.ready = true;
   }
@@ -996,7 +1036,7 @@ attn_status_t attn_prefill_fwd_chunk(const void* q, const void* k, const void* v
   const attn_status_t ds = device_state(stream, &st);
   if (ds != ATTN_OK) return ds;
   return launch_forward(q, k, v, o, lse, B, Lq, Lk, n_q, n_kv, d_h, causal, scale, stream,
-                        st->status, st->sms);
+                        st->status, st->sms, st->l2);
 }
 
 attn_status_t attn_prefill_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -1022,7 +1062,8 @@ attn_status_t attn_prefill_fwd_fp8(const void* q, const void* k, const void* v, 
   const attn_status_t ds = device_state(stream, &st);
   if (ds != ATTN_OK) return ds;
   return launch_forward(q, k, v, o, lse, B, Lq, Lk, n_q, n_kv, d_h, causal, scale, stream,
-                        st->status, st->sms, true, q_descale * k_descale, v_descale);
+                        st->status, st->sms, st->l2, true, q_descale * k_descale,
+                        v_descale);
 }
 
 const char* attn_status_string(attn_status_t status) {
@@ -1101,7 +1142,7 @@ extern "C" attn_status_t attn_prefill_fwd_noalloc(const void* q, const void* k, 
   // The status word is not cleared here: like the allocating path's word it
   // collects every wait timeout since attn_device_check last read it.
   return launch_forward(q, k, v, o, lse, B, L, L, n_q, n_kv, d_h, causal, scale, stream,
-                        st->scratch, st->sms);
+                        st->scratch, st->sms, st->l2);
 }
 
 extern "C" attn_status_t attn_selftest_wait_timeout_noalloc(int64_t spin_cycles,
