@@ -7,7 +7,8 @@ does not load the library; the first call does, and raises if it is missing.
 """
 
 from ._abi import (ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA,
-                   ATTN_ERR_TIMEOUT, load as load_library, library_path, status_string)
+                   ATTN_ERR_TIMEOUT, ATTN_ERR_CHECK, load as load_library, library_path,
+                   status_string)
 from .api import (AttnError, attn_decode, attn_decode_fwd, attn_decode_workspace_bytes,
                   attn_prefill, attn_prefill_fp8, attn_prefill_fwd, attn_prefill_fwd_chunk,
                   attn_prefill_fwd_fp8, attn_device_check, attn_prefill_grid_size,
@@ -18,7 +19,7 @@ from .api import (AttnError, attn_decode, attn_decode_fwd, attn_decode_workspace
 
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_CUDA",
-    "ATTN_ERR_TIMEOUT", "AttnError", "attn_prefill", "attn_prefill_fwd", "attn_prefill_fwd_chunk",
+    "ATTN_ERR_TIMEOUT", "ATTN_ERR_CHECK", "AttnError", "attn_prefill", "attn_prefill_fwd", "attn_prefill_fwd_chunk",
     "attn_prefill_fp8", "attn_prefill_fwd_fp8", "attn_decode", "attn_decode_fwd",
     "attn_decode_workspace_bytes", "attn_device_check", "attn_prefill_backward",
     "attn_prefill_bwd", "attn_prefill_bwd_workspace_bytes", "attn_selftest_wait_timeout",

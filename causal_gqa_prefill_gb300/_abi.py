@@ -17,6 +17,7 @@ ATTN_ERR_INVALID_ARG = 1
 ATTN_ERR_UNSUPPORTED = 2
 ATTN_ERR_CUDA = 3
 ATTN_ERR_TIMEOUT = 4
+ATTN_ERR_CHECK = 5
 
 # Every function the public header declares, with its ctypes signature.
 _SIGNATURES = {
@@ -71,6 +72,7 @@ _SIGNATURES = {
                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
                                              ctypes.c_void_p]),
     "attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "attn_debug_check_count": (ctypes.c_int64, []),
     "attn_device_check": (ctypes.c_int, [ctypes.c_void_p]),
     "attn_prefill_grid_size": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
                                                 ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),

@@ -69,11 +69,15 @@ constexpr int kOStageBytes = 8 * kOStageWarpBytes;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384;
+static_assert(kColS0 + kBN <= kColS1 && kColS1 + kBN <= kColO0 && kColO0 + 128 <= kColO1 &&
+                  kColO1 + 128 <= kTmemCols,
+              "TMEM column regions overlap or exceed the allocation");
 // A row's running maximum is only moved (and O rescaled) once the tile maximum
 // exceeds it by this many log2 units; exponentials stay <= 2^8 meanwhile, and
 // the final O / l and LSE use the same stale maximum, so the result is exact.
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kStatusTimeout = 1;
+constexpr int kStatusCheck = 2;     // a consistency check of the ATTN_DEBUG build failed
 constexpr long long kSpinLimitCycles = 1ll << 31;   // about a second at 2 GHz
 // Smallest batch of (b, kv-head) groups in the unit order, in rounds of the
 // persistent grid (decode_unit).
@@ -116,6 +120,18 @@ struct Params {
   long long spin_limit;
 };
 
+#ifdef ATTN_DEBUG
+// Debug build: how many phases each barrier's producer has started (TMA loads
+// issued, commits issued, arrival rounds begun), and how many phases each
+// waiter has consumed. A parity wait for phase k is only sound while no more
+// than phase k + 1 has been started; every wait checks that. `checks` counts
+// the checks run.
+struct DbgShadow {
+  unsigned int q_full, q_empty, kv_full[8], kv_empty[8], s_full[2], p_full[2], o_done[2];
+  unsigned int checks;
+};
+#endif
+
 struct Ctl {
   uint64_t q_full, q_empty;
   uint64_t kv_full[8], kv_empty[8];
@@ -123,7 +139,43 @@ struct Ctl {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+#ifdef ATTN_DEBUG
+  DbgShadow dbg;
+#endif
 };
+
+// Consistency checks of the ATTN_DEBUG build. The statement macros below
+// expand to nothing in the release build, whose kernels are therefore the
+// same code as without them. A failed check raises the abort flag and the
+// check bit of the status word, and the caller leaves through the same path
+// as after a wait timeout.
+#ifdef ATTN_DEBUG
+__device__ unsigned long long g_dbg_checks;   // checks run, summed at CTA exit
+
+__device__ __forceinline__ bool dbg_ok(bool cond, Ctl& ctl, const Params& p) {
+  atomicAdd(&ctl.dbg.checks, 1u);
+  if (!cond) {
+    *reinterpret_cast<volatile int*>(&ctl.abort) = 1;
+    atomicOr(p.status, kStatusCheck);
+  }
+  return cond;
+}
+// the parity wait for phase k of `field`'s barrier is sound
+#define DBG_PHASE_OK(field, k) \
+  dbg_ok(*reinterpret_cast<volatile unsigned int*>(&ctl.dbg.field) <= (k) + 1u, ctl, p)
+#define DBG_ISSUE(field) atomicAdd(&ctl.dbg.field, 1u)
+#define DBG_BREAK_UNLESS(cond) \
+  if (!(cond)) {               \
+    ok = false;                \
+    break;                     \
+  }
+#define DBG_RETURN_UNLESS(cond) \
+  if (!(cond)) return;
+#else
+#define DBG_ISSUE(field)
+#define DBG_BREAK_UNLESS(cond)
+#define DBG_RETURN_UNLESS(cond)
+#endif
 
 struct Unit {
   int b, kvh, nkv;
@@ -240,7 +292,7 @@ __global__ void __launch_bounds__(64, 1) wait_selftest_kernel(const Params p) {
 template <int D, bool F8>
 __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                           const CUtensorMap* tmV, Ctl& ctl, const Params& p,
-                          uint32_t sQ0, uint32_t sQ1, uint32_t sKV) {
+                          uint32_t sQ0, uint32_t sQ1, uint32_t sKV, uint32_t smem_end) {
   using TL = Tile<D, F8>;
   // Run by lane 0 alone: a whole warp polling the ring barriers would cost
   // the softmax warps on this SM sub-partition more issue slots than it saves.
@@ -248,11 +300,23 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
   uint32_t q_issued = 0;
   bool ok = true;
   int uc = 0;
+#ifdef ATTN_DEBUG
+  // a copy's tile must start inside its tensor (x aligned to 16 bytes) and
+  // land inside the CTA's shared memory
+  const int nB = p.groups / p.n_kv;
+  auto tma_ok = [&](uint32_t dst, int c0, int c1, int H, int c2, int rows, int c3) -> bool {
+    return dbg_ok((c0 * TL::kElemBytes) % 16 == 0 && c0 >= 0 && c0 < D && c1 >= 0 && c1 < H &&
+                      c2 >= 0 && c2 < rows && c3 >= 0 && c3 < nB && dst >= sQ0 &&
+                      dst + kBM * 128 <= smem_end,
+                  ctl, p);
+  };
+#endif
   for (int r = 0; r * static_cast<int>(gridDim.x) < p.units; ++r) {
     const int u = snake_unit(r);
     if (u >= p.units) continue;
     const Unit x = decode_unit(u, p);
     if (uc > 0 && !wait_phase(smem_addr(&ctl.q_empty), (uc - 1) & 1, ctl, p)) { ok = false; break; }
+    DBG_BREAK_UNLESS(uc == 0 || DBG_PHASE_OK(q_empty, static_cast<uint32_t>(uc - 1)))
     ++uc;
     const uint32_t qbar = smem_addr(&ctl.q_full);
     mbar_arrive_expect_tx(qbar, (x.n[0] > 0 ? 2u : 1u) * TL::kQBytes);
@@ -262,10 +326,17 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
       if (x.n[s] == 0) continue;
       const uint32_t dst = s ? sQ1 : sQ0;
 #pragma unroll
-      for (int c = 0; c < TL::kChunks; ++c)
+      for (int c = 0; c < TL::kChunks; ++c) {
+        DBG_BREAK_UNLESS(tma_ok(dst + c * kBM * 128, c * TL::kChunkElems, x.head[s], p.n_q,
+                                x.qtile[s] * kBM, p.Lq, x.b))
         tma_load_4d(dst + c * kBM * 128, tmQ, qbar, c * TL::kChunkElems, x.head[s], x.qtile[s] * kBM,
                     x.b);
+      }
     }
+#ifdef ATTN_DEBUG
+    if (!ok) break;
+#endif
+    DBG_ISSUE(q_full);
     for (int j = 0; j < x.nkv && ok; ++j) {
 #pragma unroll
       for (int kind = 0; kind < 2; ++kind) {
@@ -274,13 +345,22 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
           ok = false;
           break;
         }
+        DBG_BREAK_UNLESS(use == 0 || DBG_PHASE_OK(kv_empty[slot], use - 1))
         const uint32_t bar = smem_addr(&ctl.kv_full[slot]);
         const uint32_t dst = sKV + slot * TL::kKVBytes;
+#ifdef ATTN_DEBUG
+        bool coords = true;
+        for (int c = 0; c < TL::kChunks; ++c)
+          coords = coords && tma_ok(dst + c * kBN * 128, c * TL::kChunkElems, x.kvh, p.n_kv,
+                                    j * kBN, p.Lk, x.b);
+        DBG_BREAK_UNLESS(coords)
+#endif
         mbar_arrive_expect_tx(bar, TL::kKVBytes);
 #pragma unroll
         for (int c = 0; c < TL::kChunks; ++c)
           tma_load_4d(dst + c * kBN * 128, kind ? tmV : tmK, bar, c * TL::kChunkElems, x.kvh, j * kBN,
                       x.b);
+        DBG_ISSUE(kv_full[slot]);
         ++it;
       }
     }
@@ -337,7 +417,7 @@ __device__ __forceinline__ void issue_pv(bool leader, uint32_t d_tmem, uint32_t 
 
 template <int D, bool F8>
 __device__ void mma_role(Ctl& ctl, const Params& p, uint32_t tmem, uint32_t sQ0, uint32_t sQ1,
-                         uint32_t sKV) {
+                         uint32_t sKV, uint32_t smem_end) {
   using TL = Tile<D, F8>;
   // The whole warp runs this loop (so its control flow and descriptor math
   // stay warp-uniform); one elected lane issues every tcgen05 instruction,
@@ -346,11 +426,26 @@ __device__ void mma_role(Ctl& ctl, const Params& p, uint32_t tmem, uint32_t sQ0,
   uint32_t it = 0;
   uint32_t ph_p0 = 0, ph_p1 = 0;
   int uc = 0;
+#ifdef ATTN_DEBUG
+  // the allocation starts at lane 0, column 0; operand tiles lie inside the
+  // CTA's shared memory; phases consumed per P-ready barrier
+  uint32_t n_p0 = 0, n_p1 = 0;
+  auto smem_ok = [&](uint32_t a, uint32_t bytes) -> bool {
+    return dbg_ok(a >= sQ0 && a + bytes <= smem_end, ctl, p);
+  };
+  const bool tmem_ok = dbg_ok(tmem == 0u, ctl, p);
+#endif
   for (int r = 0; r * static_cast<int>(gridDim.x) < p.units; ++r) {
     const int u = snake_unit(r);
     if (u >= p.units) continue;
     const Unit x = decode_unit(u, p);
+#ifdef ATTN_DEBUG
+    if (!tmem_ok) break;
+#endif
     if (!wait_all(smem_addr(&ctl.q_full), uc & 1, ctl, p)) break;
+#ifdef ATTN_DEBUG
+    if (!DBG_PHASE_OK(q_full, static_cast<uint32_t>(uc))) break;
+#endif
     ++uc;
     tc_fence_after_sync();
     uint32_t v_prev = 0;
@@ -358,45 +453,84 @@ __device__ void mma_role(Ctl& ctl, const Params& p, uint32_t tmem, uint32_t sQ0,
     for (int j = 0; j < x.nkv; ++j) {
       const uint32_t ks = it % TL::kStages;
       if (!wait_all(smem_addr(&ctl.kv_full[ks]), (it / TL::kStages) & 1, ctl, p)) { ok = false; break; }
+      DBG_BREAK_UNLESS(DBG_PHASE_OK(kv_full[ks], it / TL::kStages))
       ++it;
       tc_fence_after_sync();
       const uint32_t k_smem = sKV + ks * TL::kKVBytes;
+      DBG_BREAK_UNLESS(smem_ok(k_smem, TL::kKVBytes) && smem_ok(sQ0, TL::kQBytes) &&
+                       smem_ok(sQ1, TL::kQBytes))
       if (j < x.n[0]) {
         issue_qk<D, F8>(leader, tmem + kColS0, sQ0, k_smem);
         if (leader) mma_commit(smem_addr(&ctl.s_full[0]));
+#ifdef ATTN_DEBUG
+        if (leader) DBG_ISSUE(s_full[0]);
+#endif
       }
       if (j > 0) {
         if (!wait_all(smem_addr(&ctl.p_full[1]), ph_p1, ctl, p)) { ok = false; break; }
         ph_p1 ^= 1;
+#ifdef ATTN_DEBUG
+        DBG_BREAK_UNLESS(DBG_PHASE_OK(p_full[1], n_p1))
+        ++n_p1;
+#endif
         tc_fence_after_sync();
         issue_pv<D, F8>(leader, tmem + kColO1, tmem + kColS1, sKV + v_prev * TL::kKVBytes, j - 1 > 0);
         if (leader) mma_commit(smem_addr(&ctl.kv_empty[v_prev]));
+#ifdef ATTN_DEBUG
+        if (leader) DBG_ISSUE(kv_empty[v_prev]);
+#endif
       }
       issue_qk<D, F8>(leader, tmem + kColS1, sQ1, k_smem);
       if (leader) mma_commit(smem_addr(&ctl.s_full[1]));
       if (leader) mma_commit(smem_addr(&ctl.kv_empty[ks]));
       if (leader && j == x.nkv - 1) mma_commit(smem_addr(&ctl.q_empty));
+#ifdef ATTN_DEBUG
+      if (leader) {
+        DBG_ISSUE(s_full[1]);
+        DBG_ISSUE(kv_empty[ks]);
+        if (j == x.nkv - 1) DBG_ISSUE(q_empty);
+      }
+#endif
 
       const uint32_t vs = it % TL::kStages;
       if (!wait_all(smem_addr(&ctl.kv_full[vs]), (it / TL::kStages) & 1, ctl, p)) { ok = false; break; }
+      DBG_BREAK_UNLESS(DBG_PHASE_OK(kv_full[vs], it / TL::kStages) &&
+                       smem_ok(sKV + vs * TL::kKVBytes, TL::kKVBytes))
       ++it;
       tc_fence_after_sync();
       if (j < x.n[0]) {
         if (!wait_all(smem_addr(&ctl.p_full[0]), ph_p0, ctl, p)) { ok = false; break; }
         ph_p0 ^= 1;
+#ifdef ATTN_DEBUG
+        DBG_BREAK_UNLESS(DBG_PHASE_OK(p_full[0], n_p0))
+        ++n_p0;
+#endif
         tc_fence_after_sync();
         issue_pv<D, F8>(leader, tmem + kColO0, tmem + kColS0, sKV + vs * TL::kKVBytes, j > 0);
         if (leader && j == x.n[0] - 1) mma_commit(smem_addr(&ctl.o_done[0]));
+#ifdef ATTN_DEBUG
+        if (leader && j == x.n[0] - 1) DBG_ISSUE(o_done[0]);
+#endif
       }
       v_prev = vs;
     }
     if (!ok) break;
     if (!wait_all(smem_addr(&ctl.p_full[1]), ph_p1, ctl, p)) break;
     ph_p1 ^= 1;
+#ifdef ATTN_DEBUG
+    if (!DBG_PHASE_OK(p_full[1], n_p1)) break;
+    ++n_p1;
+#endif
     tc_fence_after_sync();
     issue_pv<D, F8>(leader, tmem + kColO1, tmem + kColS1, sKV + v_prev * TL::kKVBytes, x.nkv - 1 > 0);
     if (leader) mma_commit(smem_addr(&ctl.o_done[1]));
     if (leader) mma_commit(smem_addr(&ctl.kv_empty[v_prev]));
+#ifdef ATTN_DEBUG
+    if (leader) {
+      DBG_ISSUE(o_done[1]);
+      DBG_ISSUE(kv_empty[v_prev]);
+    }
+#endif
   }
   // No MMA may still be running when TMEM is released.
   if (leader) mma_commit(smem_addr(&ctl.drain));
@@ -451,6 +585,12 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem,
   const float cc = kPos ? p.c : 1.0f;
   const uint64_t cc2 = f32x2_pack(cc, cc);
   uint32_t ph_s = 0, ph_o = 0;
+#ifdef ATTN_DEBUG
+  // the allocation starts at lane 0, column 0, so this warp's loads and
+  // stores use its own lane quarter; phases consumed per barrier
+  uint32_t n_s = 0, n_o = 0;
+  DBG_RETURN_UNLESS(dbg_ok(tmem == 0u, ctl, p))
+#endif
 
   for (int rr = 0; rr * static_cast<int>(gridDim.x) < p.units; ++rr) {
     const int u = snake_unit(rr);
@@ -468,6 +608,10 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem,
     for (int j = 0; j < n; ++j) {
       if (!__all_sync(0xffffffffu, wait_phase(bar_s, ph_s, ctl, p))) return;
       ph_s ^= 1;
+#ifdef ATTN_DEBUG
+      DBG_RETURN_UNLESS(__all_sync(0xffffffffu, DBG_PHASE_OK(s_full[slot], n_s)))
+      ++n_s;
+#endif
       tc_fence_after_sync();
       float s[128];
       {
@@ -570,10 +714,17 @@ __device__ void softmax_role(int slot, Ctl& ctl, const Params& p, uint32_t tmem,
       tmem_wait_st();
       tc_fence_before_sync();
       mbar_arrive(bar_p);
+#ifdef ATTN_DEBUG
+      if (r == 0) DBG_ISSUE(p_full[slot]);
+#endif
     }
     // Epilogue: O = acc / l (bf16, round to nearest even) and LSE in natural log.
     if (!__all_sync(0xffffffffu, wait_phase(bar_o, ph_o, ctl, p))) return;
     ph_o ^= 1;
+#ifdef ATTN_DEBUG
+    DBG_RETURN_UNLESS(__all_sync(0xffffffffu, DBG_PHASE_OK(o_done[slot], n_o)))
+    ++n_o;
+#endif
     tc_fence_after_sync();
     const float inv_l = p.o_scale / l_run;
     const bool valid = row < p.Lq;
@@ -633,6 +784,7 @@ attn_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
   __shared__ Ctl ctl;
   const uint32_t base = (smem_addr(dyn_smem) + 1023u) & ~1023u;   // swizzle atoms need 1 KiB
   const uint32_t sQ0 = base, sQ1 = base + TL::kQBytes, sKV = base + 2 * TL::kQBytes;
+  const uint32_t smem_end = smem_addr(dyn_smem) + TL::kSmemBytes;   // checked in debug builds
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -649,6 +801,9 @@ attn_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
     }
     mbar_init(smem_addr(&ctl.drain), 1);
     ctl.abort = 0;
+#ifdef ATTN_DEBUG
+    memset(&ctl.dbg, 0, sizeof(ctl.dbg));
+#endif
     fence_mbar_init();
   }
   if (warp == kLoadWarp && lane == 0) {
@@ -671,9 +826,9 @@ attn_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
     if (warp == kLoadWarp) {
-      if (lane == 0) load_role<D, F8>(&tmQ, &tmK, &tmV, ctl, p, sQ0, sQ1, sKV);
+      if (lane == 0) load_role<D, F8>(&tmQ, &tmK, &tmV, ctl, p, sQ0, sQ1, sKV, smem_end);
     } else if (warp == kMmaWarp) {
-      mma_role<D, F8>(ctl, p, tmem, sQ0, sQ1, sKV);
+      mma_role<D, F8>(ctl, p, tmem, sQ0, sQ1, sKV, smem_end);
     }
   }
 
@@ -683,6 +838,9 @@ attn_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }
+#ifdef ATTN_DEBUG
+  if (threadIdx.x == 0) atomicAdd(&g_dbg_checks, static_cast<unsigned long long>(ctl.dbg.checks));
+#endif
 }
 
 // ---------------------------------------------------------------- host side
@@ -1073,6 +1231,8 @@ const char* attn_status_string(attn_status_t status) {
     case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED: unsupported size, head dim or device";
     case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: CUDA call or kernel launch failed";
     case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a device-side wait exceeded its limit";
+    case ATTN_ERR_CHECK:
+      return "ATTN_ERR_CHECK: a device-side consistency check of the debug build failed";
   }
   return "ATTN_ERR_UNKNOWN";
 }
@@ -1095,7 +1255,21 @@ attn_status_t attn_device_check(void* stream_ptr) {
   if (status && read_and_clear(status, &word) != ATTN_OK) return ATTN_ERR_CUDA;
   if (noalloc_status && read_and_clear(noalloc_status, &noalloc_word) != ATTN_OK)
     return ATTN_ERR_CUDA;
-  return (word | noalloc_word) == 0 ? ATTN_OK : ATTN_ERR_TIMEOUT;
+  const int any = word | noalloc_word;
+  if (any == 0) return ATTN_OK;
+  return (any & kStatusCheck) ? ATTN_ERR_CHECK : ATTN_ERR_TIMEOUT;
+}
+
+int64_t attn_debug_check_count(void) {
+#ifdef ATTN_DEBUG
+  unsigned long long n = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpyFromSymbol(&n, g_dbg_checks, sizeof(n)) != cudaSuccess)
+    return -1;
+  return static_cast<int64_t>(n);
+#else
+  return -1;
+#endif
 }
 
 attn_status_t attn_selftest_wait_timeout(int64_t spin_cycles, void* stream_ptr) {

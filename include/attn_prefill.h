@@ -67,9 +67,12 @@ typedef enum {
                                 tile indexing, device that is not sm_103, a first
                                 call on a device made during stream capture */
   ATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call or the launch failed */
-  ATTN_ERR_TIMEOUT = 4       /* a kernel wait ran past its limit (reported by
+  ATTN_ERR_TIMEOUT = 4,      /* a kernel wait ran past its limit (reported by
                                 attn_device_check); outputs of that launch are
                                 undefined */
+  ATTN_ERR_CHECK = 5         /* a device-side consistency check failed (only the
+                                library built with ATTN_DEBUG runs them; reported
+                                by attn_device_check); outputs undefined */
 } attn_status_t;
 
 /*
@@ -278,6 +281,24 @@ attn_status_t attn_selftest_wait_timeout(int64_t spin_cycles, void* stream);
  * a device does attn_prefill_fwd_noalloc's set-up (refused during capture).
  */
 attn_status_t attn_selftest_wait_timeout_noalloc(int64_t spin_cycles, void* stream);
+
+/*
+ * Consistency checks of the debug build (no counterpart on the pages; a
+ * development aid). The library compiled with ATTN_DEBUG (libattn_prefill_debug.so,
+ * built beside the release library) checks, in the forward kernels, before
+ * each operation: that every TMA copy starts inside its tensor with its
+ * innermost offset 16-byte aligned and lands inside the CTA's shared memory;
+ * that the tensor-memory allocation starts at lane 0, column 0 (every warp's
+ * loads and stores then use its own lane quarter and fixed columns below
+ * 512); that every tensor-core operand tile lies inside shared memory; and
+ * that every mbarrier parity wait is sound (no more than one phase beyond the
+ * awaited one has been started). A failed check raises the kernel's abort
+ * flag (every role leaves as after a wait timeout) and attn_device_check
+ * returns ATTN_ERR_CHECK. This call returns the number of checks the debug
+ * build has run since it was loaded (synchronising the device first), or -1
+ * in the release build (which runs none) or on a CUDA error.
+ */
+int64_t attn_debug_check_count(void);
 
 /*
  * Number of persistent CTAs the forward kernel launches for these sizes on

@@ -48,6 +48,13 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_debug_library_builds_and_exports_every_declared_symbol():
+    dbg = cg.load_library(build.build(debug=True))
+    for name in _declared_functions():
+        assert hasattr(dbg, name), name
+    assert cg.status_string(cg.ATTN_ERR_CHECK).startswith("ATTN_ERR_CHECK")
+
+
 def test_status_strings(lib):
     for code in range(5):
         s = cg.status_string(code)
