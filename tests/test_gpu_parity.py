@@ -87,6 +87,27 @@ def test_workload_sampled_rows(num):
     assert torch.isfinite(o).all() and torch.isfinite(lse).all()
 
 
+def test_outputs_past_2_31_elements():
+    """One MQA layer whose Q and O hold more than 2^31 elements (4.3 GB of
+    bf16 each): the output row offsets and the tensor-map row coordinates of
+    the last heads' last tiles lie past the 32-bit element range, where an
+    index computed in 32 bits would wrap. Checked on rows of five heads at
+    the tile edges, the middle and the last rows (the last one past 2^31)."""
+    w = W.custom(1, 262500, 64, 1, 128)             # rows >= 262144 lie past 2^31 elements
+    assert (w.L - 129) * w.n_q * w.d_h >= 2 ** 31
+    q, k, v = W.make_inputs(w, "cuda", seed=4242)
+    o, lse = run_gpu(q, k, v, causal=True, scale=w.scale)
+    L = w.L
+    pos = [0, 1, 127, 128, 129, L // 2, L - 257, L - 129, L - 128, L - 2, L - 1]
+    rng = np.random.default_rng(4242)
+    rows = [(0, h, i) for h in (0, 1, 31, 62, 63)
+            for i in pos + [int(x) for x in rng.integers(0, L, 6)]]
+    err = check_rows(q, k, v, o, lse, rows, causal=True, scale=w.scale, what=w.name)
+    print(f"parity {w.name} ({len(rows)} rows): {err}")
+    del q, k, v, o, lse
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("scale", [0.0, -0.0883883, 0.5, 1e-3])
 def test_scale_values(scale):
     w = W.custom(1, 400, 4, 2, 128)
