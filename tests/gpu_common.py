@@ -141,3 +141,48 @@ def check_fp8_rows(q, k, v, o, lse, rows, descales=(1.0, 1.0, 1.0), causal=True,
     err = fp8_errors(o_sel, lse_sel, o_ref, lse_ref, o_abs)
     assert_fp8_within(err, what)
     return err
+
+
+# ----------------------------------------------------------------------------
+# backward (dQ, dK, dV)
+#
+# Per gradient G, against the fp64 oracle on the same bf16 inputs and dO:
+# ||err||_F / ||G_ref||_F <= 1e-2 and |err| <= 2^-6 max|G_ref| + 2^-8 |G_ref|
+# per element. The arithmetic behind it: P and dS are rounded to bf16 (<= 2^-9
+# relative) before the products that consume them, D comes from the bf16
+# forward output, the products accumulate in fp32 and G is rounded to bf16 at
+# the end (<= 2^-9 |G|).
+
+REL_FRO = 1e-2
+ABS_OF_MAX = 2.0 ** -6
+REL_ELEM = 2.0 ** -8
+
+
+def grad_errors(g_gpu, g_ref):
+    d = g_gpu - g_ref
+    ref_max = float(np.abs(g_ref).max()) if g_ref.size else 0.0
+    fro = float(np.linalg.norm(d) / max(np.linalg.norm(g_ref), 1e-30))
+    excess = np.abs(d) - (ABS_OF_MAX * ref_max + REL_ELEM * np.abs(g_ref))
+    return {"rel_fro": fro, "max_abs": float(np.abs(d).max()) if d.size else 0.0,
+            "ref_max": ref_max, "excess": float(excess.max()) if d.size else 0.0}
+
+
+def assert_grads(gpu, ref, what=""):
+    out = {}
+    for name, g, r in zip(("dq", "dk", "dv"), gpu, ref):
+        e = grad_errors(to_np(g), r)
+        out[name] = e
+        assert np.isfinite(e["max_abs"]), (what, name, e)
+        assert e["rel_fro"] <= REL_FRO, (what, name, e)
+        assert e["excess"] <= 0.0, (what, name, e)
+    return out
+
+
+def run_backward(q, k, v, dout, causal=True, scale=None):
+    """The product's forward (O, LSE), then its backward, through the C ABI."""
+    from causal_gqa_prefill_gb300 import attn_prefill_backward
+
+    o, lse = attn_prefill(q, k, v, causal=causal, scale=scale)
+    dq, dk, dv = attn_prefill_backward(q, k, v, o, lse, dout, causal=causal, scale=scale)
+    assert attn_device_check() == ATTN_OK
+    return dq, dk, dv

@@ -17,51 +17,15 @@ first three give errors of a few 2^-9 of the RMS of G's terms; the bounds are
   * max |err| <= 2^-6 * max |G_ref| + 2^-8 * |G_ref|   (element-wise)
 """
 
-import numpy as np
 import pytest
 import torch
 
 import oracle
-from causal_gqa_prefill_gb300 import (ATTN_OK, ATTN_ERR_UNSUPPORTED, AttnError, attn_device_check,
-                                      attn_prefill, attn_prefill_backward)
+from causal_gqa_prefill_gb300 import ATTN_ERR_UNSUPPORTED, AttnError, attn_prefill_backward
 from causal_gqa_prefill_gb300 import workloads as W
+from gpu_common import REL_FRO, assert_grads, grad_errors, run_backward, to_np
 
 pytestmark = pytest.mark.gpu
-
-REL_FRO = 1e-2
-ABS_OF_MAX = 2.0 ** -6
-REL_ELEM = 2.0 ** -8
-
-
-def to_np(t):
-    return t.float().cpu().numpy().astype(np.float64)
-
-
-def grad_errors(g_gpu, g_ref):
-    d = g_gpu - g_ref
-    ref_max = float(np.abs(g_ref).max()) if g_ref.size else 0.0
-    fro = float(np.linalg.norm(d) / max(np.linalg.norm(g_ref), 1e-30))
-    excess = np.abs(d) - (ABS_OF_MAX * ref_max + REL_ELEM * np.abs(g_ref))
-    return {"rel_fro": fro, "max_abs": float(np.abs(d).max()) if d.size else 0.0,
-            "ref_max": ref_max, "excess": float(excess.max()) if d.size else 0.0}
-
-
-def assert_grads(gpu, ref, what=""):
-    out = {}
-    for name, g, r in zip(("dq", "dk", "dv"), gpu, ref):
-        e = grad_errors(to_np(g), r)
-        out[name] = e
-        assert np.isfinite(e["max_abs"]), (what, name, e)
-        assert e["rel_fro"] <= REL_FRO, (what, name, e)
-        assert e["excess"] <= 0.0, (what, name, e)
-    return out
-
-
-def run_backward(q, k, v, dout, causal=True, scale=None):
-    o, lse = attn_prefill(q, k, v, causal=causal, scale=scale)
-    dq, dk, dv = attn_prefill_backward(q, k, v, o, lse, dout, causal=causal, scale=scale)
-    assert attn_device_check() == ATTN_OK
-    return dq, dk, dv
 
 
 def inputs(B, L, n_q, n_kv, causal=True, number=0, d_h=128):

@@ -19,9 +19,8 @@ import oracle
 from causal_gqa_prefill_gb300 import (ATTN_OK, attn_decode, attn_device_check,
                                       attn_prefill_fp8)
 from causal_gqa_prefill_gb300 import workloads as W
-from gpu_common import check_fp8_full, check_full, run_gpu
-from test_gpu_backward import assert_grads, run_backward
-from test_gpu_backward import to_np as to_f64
+from gpu_common import assert_grads, check_fp8_full, check_full, run_backward, run_gpu
+from gpu_common import to_np as to_f64
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
